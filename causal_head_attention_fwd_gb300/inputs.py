@@ -1,0 +1,139 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the oracle checks.
+
+This module holds no attention arithmetic: it only draws numbers. Both the CUDA
+path and the CPU oracle receive exactly the arrays made here.
+
+Generator (stated so it can be re-implemented anywhere):
+  * SplitMix64 stream: state_i = seed + i * 0x9E3779B97F4A7C15 (mod 2^64), i = 1, 2, ...
+    followed by the SplitMix64 finaliser (xor-shift 30, *0xBF58476D1CE4E5B9,
+    xor-shift 27, *0x94D049BB133111EB, xor-shift 31).
+  * Each normal draw consumes two consecutive words w1, w2:
+    u = ((w >> 11) + 0.5) / 2^53  in (0, 1),
+    z = sqrt(-2 ln u1) * cos(2 pi u2)   (Box-Muller, float64).
+  * x = sigma * z, rounded once to float32; for bf16 inputs the float32 value is
+    rounded once more to bf16 (round to nearest, ties to even).
+
+Workloads (shapes and distributions of the GPT-2 and ViT-B/16 attention layers):
+  qkv has shape (B, T, 3C); dout has shape (B, T, C).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+_CHUNK = 1 << 22
+
+
+def _splitmix64(seed: int, start: int, n: int) -> np.ndarray:
+    """Words start+1 .. start+n of the SplitMix64 stream for `seed`."""
+    idx = np.arange(start + 1, start + n + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + idx * _GOLDEN
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def normal_f64(seed: int, n: int) -> np.ndarray:
+    """n standard-normal float64 draws (Box-Muller on SplitMix64 words)."""
+    out = np.empty(n, dtype=np.float64)
+    scale = 1.0 / 9007199254740992.0  # 2^-53
+    for s in range(0, n, _CHUNK):
+        m = min(_CHUNK, n - s)
+        w = _splitmix64(seed, 2 * s, 2 * m)
+        u = ((w >> np.uint64(11)).astype(np.float64) + 0.5) * scale
+        u1, u2 = u[0::2], u[1::2]
+        out[s:s + m] = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
+    return out
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (nearest, ties to even); returns uint16 bit patterns."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    with np.errstate(over="ignore"):
+        r = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One attention layer configuration."""
+    name: str
+    B: int
+    T: int
+    C: int
+    NH: int
+    causal: int
+    dtype: str          # "f32" or "bf16"
+    sigma_qkv: float
+    sigma_dout: float
+    seed_qkv: int
+    seed_dout: int
+
+    @property
+    def hs(self) -> int:
+        return self.C // self.NH
+
+
+def _wl(idx, name, B, T, C, NH, causal, dtype, sq, sd):
+    return Workload(name, B, T, C, NH, causal, dtype, sq, sd, 1000 + idx, 2000 + idx)
+
+
+# The six attention-layer shapes: GPT-2 small/XL widths, a long-context GPT-2
+# layer, and ViT-B/16 (224x224 image, 16x16 patches -> 196 tokens, no mask).
+WORKLOADS = {
+    "tiny": _wl(0, "tiny", 2, 64, 128, 4, 1, "f32", 1.0, 1.0),
+    "gpt2s_f32": _wl(1, "gpt2s_f32", 4, 1024, 768, 12, 1, "f32", 0.5, 1e-2),
+    "gpt2s_bf16": _wl(2, "gpt2s_bf16", 16, 1024, 768, 12, 1, "bf16", 0.5, 1e-2),
+    "xl_bf16": _wl(3, "xl_bf16", 8, 1024, 1600, 25, 1, "bf16", 0.5, 1e-2),
+    "long_bf16": _wl(4, "long_bf16", 2, 8192, 768, 12, 1, "bf16", 0.5, 1e-2),
+    "vit_bf16": _wl(5, "vit_bf16", 256, 196, 768, 12, 0, "bf16", 0.5, 1e-2),
+}
+
+
+@dataclasses.dataclass
+class HostInputs:
+    """Host arrays for one workload.
+
+    `qkv` / `dout` hold the exact values the device sees, as float32 (for bf16
+    workloads these are bf16-representable). `qkv_dev` / `dout_dev` hold the
+    device representation: float32, or uint16 bf16 bit patterns.
+    """
+    qkv: np.ndarray
+    dout: np.ndarray
+    qkv_dev: np.ndarray
+    dout_dev: np.ndarray
+
+
+def draw(shape, sigma: float, seed: int, dtype: str):
+    """Return (exact values as float32, device representation)."""
+    n = int(np.prod(shape))
+    x = (normal_f64(seed, n) * sigma).astype(np.float32).reshape(shape)
+    if dtype == "f32":
+        return x, x
+    if dtype == "bf16":
+        bits = f32_to_bf16_bits(x)
+        return bf16_bits_to_f32(bits).reshape(shape), bits.reshape(shape)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def make_inputs(B, T, C, NH, dtype="bf16", sigma_qkv=0.5, sigma_dout=1e-2,
+                seed_qkv=1, seed_dout=2) -> HostInputs:
+    del NH  # the layout does not depend on the head split
+    qkv, qkv_dev = draw((B, T, 3 * C), sigma_qkv, seed_qkv, dtype)
+    dout, dout_dev = draw((B, T, C), sigma_dout, seed_dout, dtype)
+    return HostInputs(qkv, dout, qkv_dev, dout_dev)
+
+
+def workload_inputs(w: Workload) -> HostInputs:
+    return make_inputs(w.B, w.T, w.C, w.NH, w.dtype, w.sigma_qkv, w.sigma_dout,
+                       w.seed_qkv, w.seed_dout)
