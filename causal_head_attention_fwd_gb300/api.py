@@ -1,0 +1,119 @@
+"""Python binding of libattn.so (include/attn.h): argument marshalling only.
+
+Every function here has the name and argument order of its C counterpart.
+Tensor arguments may be torch tensors (their data_ptr() is passed) or plain
+integer device addresses; `stream` may be a torch.cuda.Stream, a raw
+cudaStream_t integer, or None for torch's current stream. All computation
+happens in the CUDA kernels behind the C ABI; there is no fallback path: if
+the library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import pathlib
+
+_LIB_PATH = pathlib.Path(__file__).resolve().parent / "libattn.so"
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_MISALIGNED = 3
+ATTN_ERR_WORKSPACE = 4
+ATTN_ERR_CUDA = 5
+ATTN_ERR_TIMEOUT = 6
+
+ATTN_F32 = 0
+ATTN_BF16 = 1
+
+EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_status_string",
+            "attn_last_device_error")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_string(status)} (status {status})")
+
+
+def _load() -> ctypes.CDLL:
+    if not _LIB_PATH.exists():
+        raise ImportError(f"libattn.so not built at {_LIB_PATH}; run "
+                          "`python -m causal_head_attention_fwd_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    vp, i, f_p, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    lib.attn_fwd.argtypes = [vp, vp, f_p, i, i, i, i, i, i, vp]
+    lib.attn_fwd.restype = i
+    lib.attn_bwd_workspace_size.argtypes = [i, i, i, i, i, i]
+    lib.attn_bwd_workspace_size.restype = sz
+    lib.attn_bwd.argtypes = [vp, vp, vp, f_p, vp, i, i, i, i, i, i, vp, sz, vp]
+    lib.attn_bwd.restype = i
+    lib.attn_status_string.argtypes = [i]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_last_device_error.argtypes = [vp]
+    lib.attn_last_device_error.restype = i
+    return lib
+
+
+_lib = _load()
+
+
+def library_path() -> str:
+    return str(_LIB_PATH)
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _dtype(d) -> int:
+    if isinstance(d, int):
+        return d
+    name = str(d)
+    if name in ("bf16", "torch.bfloat16"):
+        return ATTN_BF16
+    if name in ("f32", "torch.float32"):
+        return ATTN_F32
+    raise ValueError(f"unsupported dtype {d!r}")
+
+
+def attn_status_string(status: int) -> str:
+    return _lib.attn_status_string(int(status)).decode()
+
+
+def attn_fwd(qkv, out, lse, B, T, C, NH, causal, dtype, stream=None, check=True) -> int:
+    st = _lib.attn_fwd(_ptr(qkv), _ptr(out), _ptr(lse), B, T, C, NH, int(causal), _dtype(dtype),
+                       _stream(stream))
+    if check and st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+    return st
+
+
+def attn_bwd_workspace_size(B, T, C, NH, causal, dtype) -> int:
+    return int(_lib.attn_bwd_workspace_size(B, T, C, NH, int(causal), _dtype(dtype)))
+
+
+def attn_bwd(dout, qkv, out, lse, dqkv, B, T, C, NH, causal, dtype, workspace, workspace_bytes,
+             stream=None, check=True) -> int:
+    st = _lib.attn_bwd(_ptr(dout), _ptr(qkv), _ptr(out), _ptr(lse), _ptr(dqkv), B, T, C, NH,
+                       int(causal), _dtype(dtype), _ptr(workspace), int(workspace_bytes),
+                       _stream(stream))
+    if check and st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+    return st
+
+
+def attn_last_device_error(stream=None) -> int:
+    return int(_lib.attn_last_device_error(_stream(stream)))

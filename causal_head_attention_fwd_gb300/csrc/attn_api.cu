@@ -1,0 +1,186 @@
+// C ABI of the attention library: argument checks, TMA descriptor encoding,
+// kernel dispatch and the device error word. Declared in include/attn.h.
+#include <cstdint>
+#include <cstring>
+#include <cmath>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/attn.h"
+#include "common.cuh"
+
+namespace attn {
+
+// Declared in the kernel translation units.
+cudaError_t launch_fwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_out, float* lse,
+                            const Problem& pr, cudaStream_t stream);
+cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_dout,
+                            const CUtensorMap& map_dqkv, const void* dout, const void* out,
+                            const float* lse, void* dqkv, float* ws_D, float* ws_dq,
+                            const Problem& pr, cudaStream_t stream);
+
+static __device__ int g_error_word = 0;
+
+static constexpr int kMaxDevices = 64;
+static int* g_error_addr[kMaxDevices] = {nullptr};
+static std::mutex g_mu;
+
+int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_error_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_error_addr[dev] = static_cast<int*>(p);
+  }
+  return g_error_addr[dev];
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D map over a (B, T, W) row-major tensor of `esize`-byte elements, box
+// {box_x, box_y, 1}. Rows past T read as zero; stores past T are dropped.
+static bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int W, int T,
+                      int B, int box_x, int box_y, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)W, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)W * esize, (cuuint64_t)W * esize * (cuuint64_t)T};
+  cuuint32_t box[3] = {(cuuint32_t)box_x, (cuuint32_t)box_y, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static attn_status_t check_shape(int B, int T, int C, int NH, int causal, attn_dtype_t dtype) {
+  if (B < 1 || T < 1 || C < 1 || NH < 1) return ATTN_ERR_INVALID_ARG;
+  if (C % NH != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  const int hs = C / NH;
+  if (hs != 32 && hs != 64) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  // element counts must fit the 32-bit grid/tile arithmetic of the kernels
+  const double n3 = (double)B * T * 3.0 * C;
+  if (n3 > 9.0e15 || (double)T > 2.0e9 || (double)B * NH * ((T + 255) / 256) > 2.0e9)
+    return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+static size_t esize(attn_dtype_t dt) { return dt == ATTN_BF16 ? 2 : 4; }
+
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG: invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: head size or dtype not implemented";
+    case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED: pointer not 16-byte aligned";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: workspace missing or too small";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA call or launch failed";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a kernel's bounded wait expired";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+extern "C" attn_status_t attn_fwd(const void* qkv, void* out, float* lse, int B, int T, int C, int NH,
+                                  int causal, attn_dtype_t dtype, void* stream) {
+  attn_status_t st = check_shape(B, T, C, NH, causal, dtype);
+  if (st != ATTN_OK) return st;
+  if (!qkv || !out || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(out) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
+  const size_t e = esize(dtype);
+  if (overlaps(out, (size_t)B * T * C * e, qkv, (size_t)B * T * 3 * C * e) ||
+      overlaps(lse, (size_t)B * NH * T * 4, qkv, (size_t)B * T * 3 * C * e) ||
+      overlaps(lse, (size_t)B * NH * T * 4, out, (size_t)B * T * C * e))
+    return ATTN_ERR_INVALID_ARG;
+  Problem pr{B, T, C, NH, C / NH, causal};
+  if (!device_error_word()) return ATTN_ERR_CUDA;
+  const CUtensorMapSwizzle swz = pr.hs == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUtensorMap mq, mo;
+  if (!encode_3d(&mq, qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3 * C, T, B, pr.hs, BM, swz) ||
+      !encode_3d(&mo, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, T, B, pr.hs, BM, swz))
+    return ATTN_ERR_CUDA;
+  cudaError_t ce = launch_fwd_bf16(mq, mo, lse, pr, static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" size_t attn_bwd_workspace_size(int B, int T, int C, int NH, int causal, attn_dtype_t dtype) {
+  if (check_shape(B, T, C, NH, causal, dtype) != ATTN_OK) return 0;
+  // D (B*NH*T fp32) rounded to 256 bytes, then the fp32 dq accumulator (B*T*C)
+  const size_t d_bytes = (((size_t)B * NH * T * 4) + 255) & ~(size_t)255;
+  return d_bytes + (size_t)B * T * C * 4;
+}
+
+extern "C" attn_status_t attn_bwd(const void* dout, const void* qkv, const void* out, const float* lse,
+                                  void* dqkv, int B, int T, int C, int NH, int causal, attn_dtype_t dtype,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  attn_status_t st = check_shape(B, T, C, NH, causal, dtype);
+  if (st != ATTN_OK) return st;
+  if (!dout || !qkv || !out || !lse || !dqkv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(dout) || !aligned16(qkv) || !aligned16(out) || !aligned16(lse) || !aligned16(dqkv))
+    return ATTN_ERR_MISALIGNED;
+  const size_t need = attn_bwd_workspace_size(B, T, C, NH, causal, dtype);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_WORKSPACE;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_MISALIGNED;
+  const size_t e = esize(dtype);
+  const size_t n3 = (size_t)B * T * 3 * C * e, n1 = (size_t)B * T * C * e, nl = (size_t)B * NH * T * 4;
+  if (overlaps(dqkv, n3, qkv, n3) || overlaps(dqkv, n3, out, n1) || overlaps(dqkv, n3, dout, n1) ||
+      overlaps(dqkv, n3, lse, nl) || (workspace && overlaps(dqkv, n3, workspace, need)))
+    return ATTN_ERR_INVALID_ARG;
+  Problem pr{B, T, C, NH, C / NH, causal};
+  if (!device_error_word()) return ATTN_ERR_CUDA;
+  const CUtensorMapSwizzle swz = pr.hs == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUtensorMap mq, md, mg;
+  if (!encode_3d(&mq, qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3 * C, T, B, pr.hs, BM, swz) ||
+      !encode_3d(&md, dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, T, B, pr.hs, BM, swz) ||
+      !encode_3d(&mg, dqkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3 * C, T, B, pr.hs, BM, swz))
+    return ATTN_ERR_CUDA;
+  float* ws_D = static_cast<float*>(workspace);
+  float* ws_dq = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          ((((size_t)B * NH * T * 4) + 255) & ~(size_t)255));
+  cudaError_t ce = launch_bwd_bf16(mq, md, mg, dout, out, lse, dqkv, ws_D, ws_dq, pr,
+                                   static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" attn_status_t attn_last_device_error(void* stream) {
+  int* addr = device_error_word();
+  if (!addr) return ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, addr, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyAsync(addr, &zero, sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  return v == 0 ? ATTN_OK : (v == ATTN_ERR_TIMEOUT ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA);
+}

@@ -1,0 +1,44 @@
+// Shared definitions of the attention kernels and their host launchers.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int BM = 128;   // query rows per tile (TMEM lanes)
+constexpr int BN = 128;   // keys per tile
+
+// Swizzle geometry of a [rows][HS] bf16 tile: HS=64 -> 128-byte rows (SW128),
+// HS=32 -> 64-byte rows (SW64). One swizzle atom is 8 rows.
+template <int HS>
+struct TileGeom {
+  static constexpr int ROW_BYTES = HS * 2;
+  static constexpr int ATOM_BYTES = 8 * ROW_BYTES;
+  static constexpr uint32_t SWZ = (HS == 64) ? SWZ_128B : SWZ_64B;
+  static constexpr int TILE_BYTES = BM * ROW_BYTES;   // 128 rows
+  static_assert(HS == 32 || HS == 64, "head size must be 32 or 64");
+};
+
+// Byte offset of the 16-byte chunk `c` of row `r` inside a swizzled tile.
+template <int HS>
+__device__ __forceinline__ uint32_t swz_chunk_offset(int r, int c) {
+  if constexpr (HS == 64) {
+    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+  } else {
+    return (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+  }
+}
+
+// Host-side view of one call (already validated).
+struct Problem {
+  int B, T, C, NH, hs, causal;
+};
+
+// Device address of the library's error word (0 = fine, otherwise an
+// attn_status_t code written by a kernel whose bounded wait gave up).
+int* device_error_word();
+
+}  // namespace attn

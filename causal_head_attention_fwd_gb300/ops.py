@@ -1,0 +1,83 @@
+"""Torch-facing convenience layer over the C ABI.
+
+Allocates outputs and workspace with torch (device memory and streams only)
+and calls attn_fwd / attn_bwd; the arithmetic runs in the library's kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import api
+
+_DT = {torch.bfloat16: api.ATTN_BF16, torch.float32: api.ATTN_F32}
+
+
+def upload(arr, dtype: str, device="cuda", pin: bool = False) -> torch.Tensor:
+    """Host array in device representation (float32, or uint16 bf16 bits) -> torch tensor."""
+    import numpy as np
+    a = np.ascontiguousarray(arr)
+    if dtype == "bf16":
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    elif dtype == "f32":
+        t = torch.from_numpy(a.astype(np.float32, copy=False))
+    else:
+        raise ValueError(dtype)
+    if pin:
+        return t.pin_memory()
+    return t.to(device)
+
+
+def download_f64(t: torch.Tensor):
+    """Device tensor -> float64 numpy array (exact widening of bf16/fp32)."""
+    return t.detach().float().cpu().double().numpy()
+
+
+def _shape(qkv: torch.Tensor, n_head: int):
+    if qkv.dim() != 3 or qkv.shape[2] % 3 != 0:
+        raise ValueError("qkv must have shape (B, T, 3C)")
+    if not qkv.is_contiguous():
+        raise ValueError("qkv must be contiguous")
+    B, T, C3 = qkv.shape
+    return B, T, C3 // 3, n_head
+
+
+def attention_forward(qkv: torch.Tensor, n_head: int, causal: bool = True, out=None, lse=None,
+                      stream=None):
+    """out (B, T, C) in qkv's dtype and lse (B, NH, T) fp32."""
+    B, T, C, NH = _shape(qkv, n_head)
+    if out is None:
+        out = torch.empty((B, T, C), dtype=qkv.dtype, device=qkv.device)
+    if lse is None:
+        lse = torch.empty((B, NH, T), dtype=torch.float32, device=qkv.device)
+    api.attn_fwd(qkv, out, lse, B, T, C, NH, int(causal), _DT[qkv.dtype], stream)
+    return out, lse
+
+
+class Workspace:
+    """Reusable device scratch buffer for attn_bwd (grown on demand)."""
+
+    def __init__(self):
+        self.buf = None
+
+    def get(self, nbytes: int, device) -> torch.Tensor:
+        if nbytes == 0:
+            return None
+        if self.buf is None or self.buf.numel() < nbytes or self.buf.device != torch.device(device):
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        return self.buf
+
+
+_default_ws = Workspace()
+
+
+def attention_backward(dout, qkv, out, lse, n_head: int, causal: bool = True, dqkv=None,
+                       workspace: Workspace | None = None, stream=None):
+    """dqkv (B, T, 3C) in qkv's dtype, written with =."""
+    B, T, C, NH = _shape(qkv, n_head)
+    if dqkv is None:
+        dqkv = torch.empty_like(qkv)
+    dt = _DT[qkv.dtype]
+    nbytes = api.attn_bwd_workspace_size(B, T, C, NH, int(causal), dt)
+    ws = (workspace or _default_ws).get(nbytes, qkv.device)
+    api.attn_bwd(dout, qkv, out, lse, dqkv, B, T, C, NH, int(causal), dt, ws, nbytes, stream)
+    return dqkv

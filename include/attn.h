@@ -1,0 +1,102 @@
+/*
+ * attn.h - C ABI of the GB300 (sm_103a) multi-head self-attention library
+ * (libattn.so): forward and backward of GPT-2-style attention on the
+ * interleaved (B, T, 3C) qkv layout.
+ *
+ * Operation (llm.c dev/cuda/attention_backward.cu, attention_forward_cpu and
+ * attention_backward_cpu; "Umakini wa kujitegemea, kerneli za CUDA na
+ * FlashAttention", sections 1 and 3):
+ *   hs = C / NH, scale = 1 / sqrt(hs).
+ *   For batch b, head h, query t: q_t = qkv[b, t, h*hs : h*hs+hs],
+ *   k_j = qkv[b, j, C + h*hs : ...], v_j = qkv[b, j, 2C + h*hs : ...].
+ *   s_tj = q_t . k_j;  J(t) = {0..t} if causal else {0..T-1};
+ *   att_tj = exp(scale*s_tj) / sum_{j' in J(t)} exp(scale*s_tj') on J(t), 0 elsewhere;
+ *   out[b, t, h*hs + i] = sum_j att_tj v_j[i];
+ *   lse[b, h, t] = ln sum_{j in J(t)} exp(scale*s_tj)   (natural log).
+ *
+ * Conventions for every call:
+ *   - All data pointers are DEVICE pointers owned by the caller. The library
+ *     never allocates, frees or keeps them; it caches only device properties.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Every call is asynchronous on that stream.
+ *   - Tensors are dense, row-major, C-contiguous, in the shapes given below.
+ *   - Element type of qkv, out, dout and dqkv is `dtype`; lse, and the
+ *     backward workspace, are fp32.
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns an error status and launches nothing. The library
+ *     never exits or asserts.
+ *   - Supported: T >= 1, B >= 1, NH >= 1, C % NH == 0, hs in {32, 64},
+ *     causal in {0, 1}, dtype ATTN_BF16 or ATTN_F32, every pointer 16-byte
+ *     aligned.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, C % NH != 0, aliasing */
+  ATTN_ERR_UNSUPPORTED = 2,   /* head size or dtype this build does not implement */
+  ATTN_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+  ATTN_ERR_WORKSPACE = 4,     /* backward workspace missing or too small */
+  ATTN_ERR_CUDA = 5,          /* a CUDA runtime/driver call or launch failed */
+  ATTN_ERR_TIMEOUT = 6        /* a kernel's bounded wait expired (see attn_last_device_error) */
+} attn_status_t;
+
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+/*
+ * Forward (llm.c attention_forward_cpu, passes 1-4; FlashAttention tiling and
+ * online softmax of "Umakini wa kujitegemea ... FlashAttention" section 3).
+ *   qkv : (B, T, 3C) dtype, read only.
+ *   out : (B, T, C)  dtype, fully overwritten.
+ *   lse : (B, NH, T) fp32, fully overwritten; the row statistic the backward needs.
+ * The (B, NH, T, T) attention matrix is never materialised.
+ */
+attn_status_t attn_fwd(const void* qkv, void* out, float* lse, int B, int T, int C, int NH,
+                       int causal, attn_dtype_t dtype, void* stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for this problem (0 if none).
+ * Returns 0 also for arguments attn_bwd would reject.
+ */
+size_t attn_bwd_workspace_size(int B, int T, int C, int NH, int causal, attn_dtype_t dtype);
+
+/*
+ * Backward (llm.c attention_backward_cpu; softmax step in the row-sum form of
+ * its softmax_autoregressive_backward_kernel7: dpreatt = scale*att*(datt - D)).
+ *   dout : (B, T, C)  dtype, read only.
+ *   qkv  : (B, T, 3C) dtype, the forward's input, read only.
+ *   out  : (B, T, C)  dtype, the forward's output, read only.
+ *   lse  : (B, NH, T) fp32, the forward's row statistic, read only.
+ *   dqkv : (B, T, 3C) dtype, fully overwritten with = (an activation gradient,
+ *          "llm.c 的中文注解" section 1.1): [dq | dk | dv] in the qkv layout.
+ *          Must not overlap qkv, out, dout, lse or the workspace.
+ *   workspace : device buffer of at least attn_bwd_workspace_size(...) bytes,
+ *          256-byte aligned, owned by the caller; contents on entry do not
+ *          matter and are garbage on return.
+ */
+attn_status_t attn_bwd(const void* dout, const void* qkv, const void* out, const float* lse,
+                       void* dqkv, int B, int T, int C, int NH, int causal, attn_dtype_t dtype,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word that the
+ * kernels set when a bounded wait expires. Returns ATTN_OK, ATTN_ERR_TIMEOUT,
+ * or ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+attn_status_t attn_last_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

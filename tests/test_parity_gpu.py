@@ -1,0 +1,175 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 CPU oracle.
+
+Both sides receive the same seeded inputs (bf16 values widened exactly for the
+oracle). Tolerance rule, applied to the whole tensor:
+    max |gpu - oracle| <= tol * max |oracle|
+with tol = 2e-2 for bf16 inputs (out and dqkv). lse is an fp32 row statistic
+computed from exact bf16 products with fp32 accumulation; its absolute error is
+a few 1e-6 in practice, so 1e-3 absolute leaves ample margin while still
+catching a wrong scale, base or mask (those move lse by >= 1e-2).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from causal_head_attention_fwd_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-2}
+LSE_ABS = 1e-3
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from causal_head_attention_fwd_gb300 import build
+    build.build()
+    from causal_head_attention_fwd_gb300 import api, ops
+    return torch, api, ops
+
+
+def _rel(a, ref):
+    den = np.max(np.abs(ref))
+    return float(np.max(np.abs(a - ref)) / (den if den > 0 else 1.0))
+
+
+def _run(env, B, T, C, NH, causal, dtype="bf16", sq=0.5, sd=1e-2, seed=0):
+    torch, api, ops = env
+    host = inputs.make_inputs(B, T, C, NH, dtype, sq, sd, 100 + seed, 200 + seed)
+    qkv = ops.upload(host.qkv_dev, dtype)
+    dout = ops.upload(host.dout_dev, dtype)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    out = torch.full((B, T, C), float("nan"), dtype=tdt, device="cuda")
+    lse = torch.full((B, NH, T), float("nan"), dtype=torch.float32, device="cuda")
+    dqkv = torch.full((B, T, 3 * C), float("nan"), dtype=tdt, device="cuda")
+    ops.attention_forward(qkv, NH, bool(causal), out=out, lse=lse)
+    ops.attention_backward(dout, qkv, out, lse, NH, bool(causal), dqkv=dqkv)
+    torch.cuda.synchronize()
+    assert api.attn_last_device_error() == api.ATTN_OK
+    return host, ops.download_f64(out), ops.download_f64(lse), ops.download_f64(dqkv)
+
+
+SHAPES = [
+    # B, T, C, NH, causal         (hs = C/NH; T spans one tile, several tiles, ragged tails)
+    (1, 1, 128, 2, 1), (1, 1, 128, 2, 0),
+    (2, 17, 128, 2, 1), (2, 64, 128, 4, 1), (2, 127, 64, 1, 0),
+    (1, 128, 128, 2, 1), (1, 129, 128, 4, 1), (2, 196, 128, 2, 0),
+    (1, 255, 64, 1, 1), (1, 256, 64, 1, 0), (1, 257, 64, 1, 1),
+    (1, 600, 64, 2, 1), (1, 1000, 128, 2, 1), (1, 1000, 128, 2, 0),
+]
+
+
+@pytest.mark.parametrize("B,T,C,NH,causal", SHAPES)
+def test_parity_all_heads(env, B, T, C, NH, causal):
+    host, out, lse, dqkv = _run(env, B, T, C, NH, causal, seed=T + C)
+    ref_out, ref_lse = oracle.forward(host.qkv, B, T, C, NH, bool(causal))
+    ref_dqkv = oracle.backward(host.dout, host.qkv, B, T, C, NH, bool(causal))
+    assert np.isfinite(out).all() and np.isfinite(lse).all() and np.isfinite(dqkv).all()
+    e_out = _rel(out, ref_out)
+    assert e_out <= TOL["bf16"], f"out rel err {e_out:.3e}"
+    assert np.max(np.abs(lse - ref_lse)) <= LSE_ABS
+    for name, sl in (("dq", slice(0, C)), ("dk", slice(C, 2 * C)), ("dv", slice(2 * C, 3 * C))):
+        e = _rel(dqkv[:, :, sl], ref_dqkv[:, :, sl])
+        assert e <= TOL["bf16"], f"{name} rel err {e:.3e}"
+    assert _rel(dqkv, ref_dqkv) <= TOL["bf16"]
+
+
+def test_parity_unit_variance_hs32(env):
+    """The tiny workload's distribution (N(0,1) qkv and dout) on its shape, bf16 inputs."""
+    B, T, C, NH = 2, 64, 128, 4
+    host, out, lse, dqkv = _run(env, B, T, C, NH, 1, sq=1.0, sd=1.0, seed=5)
+    ref_out, ref_lse = oracle.forward(host.qkv, B, T, C, NH, True)
+    ref_dqkv = oracle.backward(host.dout, host.qkv, B, T, C, NH, True)
+    assert _rel(out, ref_out) <= TOL["bf16"]
+    assert np.max(np.abs(lse - ref_lse)) <= LSE_ABS
+    assert _rel(dqkv, ref_dqkv) <= TOL["bf16"]
+
+
+def test_first_row_is_v0_and_dq0_small(env):
+    """Causal row 0 attends only to key 0: out = v_0 exactly (bf16), dq_0 ~ 0."""
+    B, T, C, NH = 2, 300, 128, 2
+    host, out, _, dqkv = _run(env, B, T, C, NH, 1, seed=9)
+    np.testing.assert_array_equal(out[:, 0, :], host.qkv[:, 0, 2 * C:].astype(np.float64))
+    assert np.max(np.abs(dqkv[:, 0, :C])) <= 1e-3 * np.max(np.abs(dqkv[:, :, :C]))
+
+
+def test_outputs_fully_overwritten_and_no_out_of_bounds_writes(env):
+    """Outputs live inside larger buffers pre-filled with a sentinel: the region
+    must be fully written (no NaN left) and the guard bands untouched."""
+    torch, api, ops = env
+    B, T, C, NH, G = 2, 333, 128, 2, 4096
+    host = inputs.make_inputs(B, T, C, NH, "bf16", 0.5, 1e-2, 77, 78)
+    qkv = ops.upload(host.qkv_dev, "bf16")
+    dout = ops.upload(host.dout_dev, "bf16")
+    n_out, n_lse, n_d = B * T * C, B * NH * T, B * T * 3 * C
+    big_out = torch.full((n_out + 2 * G,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    big_lse = torch.full((n_lse + 2 * G,), float("nan"), dtype=torch.float32, device="cuda")
+    big_d = torch.full((n_d + 2 * G,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = big_out[G:G + n_out].view(B, T, C)
+    lse = big_lse[G:G + n_lse].view(B, NH, T)
+    dqkv = big_d[G:G + n_d].view(B, T, 3 * C)
+    ops.attention_forward(qkv, NH, True, out=out, lse=lse)
+    ops.attention_backward(dout, qkv, out, lse, NH, True, dqkv=dqkv)
+    torch.cuda.synchronize()
+    for big, n in ((big_out, n_out), (big_lse, n_lse), (big_d, n_d)):
+        assert not torch.isnan(big[G:G + n]).any()
+        assert torch.isnan(big[:G]).all() and torch.isnan(big[G + n:]).all()
+
+
+def test_repeat_runs_deterministic_where_designed(env):
+    """Forward and dK/dV have a fixed summation order: bit-identical reruns.
+    dQ is reduced with atomics: reruns agree within the tolerance only."""
+    torch, api, ops = env
+    B, T, C, NH = 2, 700, 128, 2
+    host = inputs.make_inputs(B, T, C, NH, "bf16", 0.5, 1e-2, 31, 32)
+    qkv = ops.upload(host.qkv_dev, "bf16")
+    dout = ops.upload(host.dout_dev, "bf16")
+    o1, l1 = ops.attention_forward(qkv, NH, True)
+    o2, l2 = ops.attention_forward(qkv, NH, True)
+    d1 = ops.attention_backward(dout, qkv, o1, l1, NH, True)
+    d2 = ops.attention_backward(dout, qkv, o1, l1, NH, True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(d1[:, :, C:], d2[:, :, C:])
+    dq1, dq2 = d1[:, :, :C].float(), d2[:, :, :C].float()
+    assert (dq1 - dq2).abs().max().item() <= 1e-2 * dq1.abs().max().item()
+
+
+FULL = ["gpt2s_bf16", "xl_bf16", "long_bf16", "vit_bf16"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_heads(env, name):
+    """Full workload sizes, in the launch configuration the benchmark times;
+    the oracle checks a seeded sample of (b, h) heads (heads are independent,
+    so each sampled head is an exact check of that head)."""
+    torch, api, ops = env
+    w = inputs.WORKLOADS[name]
+    host = inputs.workload_inputs(w)
+    qkv = ops.upload(host.qkv_dev, w.dtype)
+    dout = ops.upload(host.dout_dev, w.dtype)
+    out, lse = ops.attention_forward(qkv, w.NH, bool(w.causal))
+    dqkv = ops.attention_backward(dout, qkv, out, lse, w.NH, bool(w.causal))
+    torch.cuda.synchronize()
+    assert api.attn_last_device_error() == api.ATTN_OK
+    rng = np.random.default_rng(w.seed_qkv)
+    n_heads = 1 if w.T > 4096 else 3
+    heads = [(int(rng.integers(w.B)), int(rng.integers(w.NH))) for _ in range(n_heads)]
+    hs, C = w.hs, w.C
+    for b, h in heads:
+        x = host.qkv[b:b + 1].astype(np.float64)
+        d = host.dout[b:b + 1].astype(np.float64)
+        ref_out, ref_lse = oracle.forward(x, 1, w.T, C, w.NH, bool(w.causal), heads=[(0, h)])
+        ref_d = oracle.backward(d, x, 1, w.T, C, w.NH, bool(w.causal), heads=[(0, h)])
+        cols = slice(h * hs, (h + 1) * hs)
+        g_out = ops.download_f64(out[b, :, cols])
+        assert _rel(g_out, ref_out[0, :, cols]) <= TOL["bf16"]
+        assert np.max(np.abs(ops.download_f64(lse[b, h]) - ref_lse[0, h])) <= LSE_ABS
+        for off in (0, C, 2 * C):
+            sl = slice(off + h * hs, off + (h + 1) * hs)
+            assert _rel(ops.download_f64(dqkv[b, :, sl]), ref_d[0, :, sl]) <= TOL["bf16"], (b, h, off)
+    # every row of every head is finite
+    assert torch.isfinite(out.float()).all() and torch.isfinite(dqkv.float()).all()
