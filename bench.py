@@ -1,0 +1,379 @@
+"""Benchmark: causal multi-head attention forward + backward on one GB300.
+
+One step = attn_fwd + attn_bwd (every kernel of the hot path) over one batch
+of the GPT-2 small attention layer, bf16: B=16, T=1024, C=768, NH=12 (hs=64),
+causal. Metric: causal-adjusted TFLOP/s, FLOPs counted the FlashAttention way:
+fwd = 4*B*NH*T^2*hs/2, bwd = 2.5*fwd, step = 3.5*fwd.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints ONE JSON line (rank 0). For N>1 launch with torch.distributed.run; each
+rank runs its own independent batch (weak scaling, no collective on the data
+path; one barrier and a max-reduction of the timing only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import pathlib
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = pathlib.Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+WORKLOAD = "gpt2s_bf16"
+METRIC = "attention fwd+bwd causal TFLOP/s at 1 GB300 and % of dense tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FLUSH_BYTES = 512 << 20   # > 129 MB L2
+
+
+# ----------------------------------------------------------------------------- helpers
+def flops(B, T, C, NH, causal):
+    hs = C // NH
+    fwd = 4.0 * B * NH * T * T * hs * (0.5 if causal else 1.0)
+    return {"fwd": fwd, "bwd": 2.5 * fwd, "step": 3.5 * fwd}
+
+
+def algo_bytes(B, T, C, NH, e):
+    """Algorithmic HBM bytes: fwd reads qkv, writes out + lse; bwd reads qkv, out,
+    dout, lse, writes dqkv and D."""
+    btc = B * T * C
+    return {"fwd": 4 * btc * e + 4 * B * NH * T, "bwd": 8 * btc * e + 8 * B * NH * T}
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a scalar over all ranks (identity for world == 1)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: float, t_ms_rank: float, world: int, device=None):
+    """Whole-job throughput: units over all ranks / the slowest rank's time."""
+    t = reduce_max(t_ms_rank, world, device)
+    return units_per_rank * world / (t * 1e-3), t
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[2 + i] == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+_CPU_CHILD = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+import numpy as np
+import oracle
+from causal_head_attention_fwd_gb300 import inputs
+w = inputs.WORKLOADS[sys.argv[2]]
+budget = float(sys.argv[3]); max_heads = int(sys.argv[4])
+x, _ = inputs.draw((1, w.T, 3 * w.C), w.sigma_qkv, w.seed_qkv, w.dtype)
+d, _ = inputs.draw((1, w.T, w.C), w.sigma_dout, w.seed_dout, w.dtype)
+x = x.astype(np.float64); d = d.astype(np.float64)
+heads, t0 = 0, time.perf_counter()
+step_times = []
+while heads < max_heads and (time.perf_counter() - t0) < budget:
+    h = heads % w.NH
+    s = time.perf_counter()
+    oracle.forward(x, 1, w.T, w.C, w.NH, bool(w.causal), heads=[(0, h)])
+    oracle.backward(d, x, 1, w.T, w.C, w.NH, bool(w.causal), heads=[(0, h)])
+    step_times.append(time.perf_counter() - s)
+    heads += 1
+print(json.dumps({"heads": heads, "seconds": time.perf_counter() - t0, "step_times": step_times}))
+"""
+
+
+def run_oracle_child(workload: str, budget_s: float, max_heads: int):
+    cores = os.cpu_count() or 1
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(cores)
+    r = subprocess.run([sys.executable, "-c", _CPU_CHILD, str(ROOT), workload, str(budget_s), str(max_heads)],
+                       capture_output=True, text=True, env=env, timeout=min(budget_s * 4 + 600, 7200))
+    if r.returncode != 0:
+        raise RuntimeError("oracle child failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1]), cores
+
+
+def cpu_baseline(workload: str, budget_s: float = 15.0):
+    from causal_head_attention_fwd_gb300 import inputs
+    w = inputs.WORKLOADS[workload]
+    res, cores = run_oracle_child(workload, budget_s, 10_000)
+    f_head = flops(1, w.T, w.C, w.NH, w.causal)["step"] / w.NH
+    value = res["heads"] * f_head / res["seconds"] / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{res['heads']} (b,h) heads of {workload} (of {w.B * w.NH}), fwd+bwd, "
+                      f"float64 numpy oracle, {res['seconds']:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step = fwd+bwd of one (b, h) head."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from causal_head_attention_fwd_gb300 import inputs
+    w = inputs.WORKLOADS[WORKLOAD]
+    res, cores = run_oracle_child(WORKLOAD, 1e9, args.warmup + args.steps)
+    times = res["step_times"][args.warmup:]
+    f_head = flops(1, w.T, w.C, w.NH, w.causal)["step"] / w.NH
+    t = sum(times) / len(times)
+    value = f_head / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"one (b,h) head of {WORKLOAD} per step (1/{w.B * w.NH} of the batch), "
+                                   "fwd+bwd, float64 numpy oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(w):
+    return {"workload": f"{w.name}: GPT-2 small attention layer, B={w.B} T={w.T} C={w.C} NH={w.NH} "
+                        f"hs={w.hs}, causal, bf16 qkv~N(0,{w.sigma_qkv}^2) dout~N(0,{w.sigma_dout}^2)",
+            "B": w.B, "T": w.T, "C": w.C, "NH": w.NH, "causal": w.causal,
+            "l2": "flushed between timed steps (512 MiB write)"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    from causal_head_attention_fwd_gb300 import build, inputs
+    build.build()
+    from causal_head_attention_fwd_gb300 import api, ops
+
+    w = inputs.WORKLOADS[WORKLOAD]
+    B, T, C, NH = w.B, w.T, w.C, w.NH
+    host = inputs.make_inputs(B, T, C, NH, w.dtype, w.sigma_qkv, w.sigma_dout,
+                              w.seed_qkv + 7919 * rank, w.seed_dout + 7919 * rank)
+    qkv = ops.upload(host.qkv_dev, "bf16", dev)
+    dout = ops.upload(host.dout_dev, "bf16", dev)
+    out = torch.empty((B, T, C), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, NH, T), dtype=torch.float32, device=dev)
+    dqkv = torch.empty_like(qkv)
+    ws_bytes = api.attn_bwd_workspace_size(B, T, C, NH, 1, api.ATTN_BF16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        api.attn_fwd(qkv, out, lse, B, T, C, NH, 1, api.ATTN_BF16, stream)
+        api.attn_bwd(dout, qkv, out, lse, dqkv, B, T, C, NH, 1, api.ATTN_BF16, ws, ws_bytes, stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def timed(n, body):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        barrier()
+        for a, b in ev:
+            flush.fill_(1.0)            # evict L2 between steps (not timed)
+            a.record(stream)
+            body()
+            b.record(stream)
+        barrier()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if api.attn_last_device_error(stream) != api.ATTN_OK:
+        raise RuntimeError("device error during warm-up")
+
+    # ---- main timed region (uninstrumented)
+    with ClockSampler(local_rank) as cs:
+        times = timed(args.steps, step)
+    clocks = cs.summary()
+    if api.attn_last_device_error(stream) != api.ATTN_OK:
+        raise RuntimeError("device error in the timed region")
+    t_ms = sum(times) / len(times)
+    f = flops(B, T, C, NH, 1)
+    value_flops, t_max = aggregate(f["step"], t_ms, world, dev)
+    value = value_flops / 1e12
+
+    # ---- per-kernel device times (library event profiling), same workload
+    api.attn_profile_reset()
+    api.attn_profile_enable(True)
+    timed(max(20, min(args.steps, 200)), step)
+    api.attn_profile_enable(False)
+    kern = {}
+    for kid, name in api.KERNEL_NAMES.items():
+        ms, n = api.attn_profile_read(kid)
+        kern[name] = {"launches": n, "avg_ms": ms / max(n, 1)}
+    tot = sum(k["avg_ms"] for k in kern.values())
+    for k in kern.values():
+        k["share"] = k["avg_ms"] / tot if tot > 0 else None
+    peaks, peak_src = load_peaks()
+    dom = max(kern, key=lambda k: kern[k]["avg_ms"])
+    dom_flops = {"attn_fwd_kernel": f["fwd"], "attn_bwd_kernel": f["bwd"]}.get(dom)
+    peak_tf = float(peaks["bf16_tflops"])
+    if dom_flops is not None:
+        ach = dom_flops / (kern[dom]["avg_ms"] * 1e-3) / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
+                    "frac": ach / peak_tf, "traffic": None,
+                    "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
+                    if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16"}
+    else:
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": float(peaks["hbm_gbs"]),
+                    "unit": "GB/s", "frac": None, "traffic": None}
+    traffic_file = ROOT / "profiles" / "traffic.json"
+    if traffic_file.exists():
+        tr = json.loads(traffic_file.read_text()).get(dom)
+        if tr and tr.get("source_hash") == kernel_source_hash():
+            roofline["traffic"] = tr["bytes_per_launch"]
+    fwd_ms = kern["attn_fwd_kernel"]["avg_ms"]
+    bwd_ms = sum(kern[k]["avg_ms"] for k in ("attn_bwd_pre", "attn_bwd_kernel", "attn_bwd_dq_out"))
+    ab = algo_bytes(B, T, C, NH, 2)
+
+    # ---- end to end through the public API with host buffers
+    h_qkv = ops.upload(host.qkv_dev, "bf16", pin=True)
+    h_dout = ops.upload(host.dout_dev, "bf16", pin=True)
+    h_out = torch.empty((B, T, C), dtype=torch.bfloat16).pin_memory()
+    h_dqkv = torch.empty((B, T, 3 * C), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        qkv.copy_(h_qkv, non_blocking=True)
+        dout.copy_(h_dout, non_blocking=True)
+        ops.attention_forward(qkv, NH, True, out=out, lse=lse, stream=stream)
+        ops.attention_backward(dout, qkv, out, lse, NH, True, dqkv=dqkv, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+        h_dqkv.copy_(dqkv, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    e2e_times = timed(max(20, min(args.steps, 200)), e2e_step)
+    e2e_ms = sum(e2e_times) / len(e2e_times)
+    e2e_val, _ = aggregate(f["step"], e2e_ms, world, dev)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(w),
+        "pct_of_peak": value / peak_tf,
+        "fwd_tflops": f["fwd"] / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": f["bwd"] / (bwd_ms * 1e-3) / 1e12,
+        "fwd_hbm_gbs": ab["fwd"] / (fwd_ms * 1e-3) / 1e9, "bwd_hbm_gbs": ab["bwd"] / (bwd_ms * 1e-3) / 1e9,
+        "roofline": roofline, "kernels": kern,
+        "e2e": {"value": e2e_val / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(qkv.numel() * 2 + dout.numel() * 2),
+                "d2h_bytes_per_step": int(out.numel() * 2 + dqkv.numel() * 2),
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(WORKLOAD)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources; ties a stored ncu traffic figure to the kernel it measured."""
+    import hashlib
+    h = hashlib.sha256()
+    for p in sorted((ROOT / "causal_head_attention_fwd_gb300" / "csrc").glob("*")):
+        h.update(p.name.encode())
+        h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+if __name__ == "__main__":
+    sys.exit(main())
