@@ -26,7 +26,16 @@ ATTN_F32 = 0
 ATTN_BF16 = 1
 
 EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_status_string",
-            "attn_last_device_error")
+            "attn_last_device_error", "attn_profile_enable", "attn_profile_reset",
+            "attn_profile_read", "attn_bwd_noalloc")
+
+# size of the fixed scratch array attn_bwd_noalloc uses (ATTN_NOALLOC_SCRATCH_BYTES)
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+# kernel ids of attn_profile_read
+K_FWD, K_BWD_PRE, K_BWD_MAIN, K_BWD_DQ = 0, 1, 2, 3
+KERNEL_NAMES = {K_FWD: "attn_fwd_kernel", K_BWD_PRE: "attn_bwd_pre",
+                K_BWD_MAIN: "attn_bwd_kernel", K_BWD_DQ: "attn_bwd_dq_out"}
 
 
 class AttnError(RuntimeError):
@@ -51,6 +60,15 @@ def _load() -> ctypes.CDLL:
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_last_device_error.argtypes = [vp]
     lib.attn_last_device_error.restype = i
+    lib.attn_profile_enable.argtypes = [i]
+    lib.attn_profile_enable.restype = i
+    lib.attn_profile_reset.argtypes = []
+    lib.attn_profile_reset.restype = i
+    lib.attn_profile_read.argtypes = [i, ctypes.POINTER(ctypes.c_double),
+                                      ctypes.POINTER(ctypes.c_longlong)]
+    lib.attn_profile_read.restype = i
+    lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, f_p, vp, i, i, i, i, i, i, vp]
+    lib.attn_bwd_noalloc.restype = i
     return lib
 
 
@@ -117,3 +135,35 @@ def attn_bwd(dout, qkv, out, lse, dqkv, B, T, C, NH, causal, dtype, workspace, w
 
 def attn_last_device_error(stream=None) -> int:
     return int(_lib.attn_last_device_error(_stream(stream)))
+
+
+def attn_profile_enable(enable: bool) -> None:
+    st = _lib.attn_profile_enable(int(bool(enable)))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_profile_enable")
+
+
+def attn_profile_reset() -> None:
+    st = _lib.attn_profile_reset()
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_profile_reset")
+
+
+def attn_profile_read(kernel_id: int):
+    """(total device ms, launch count) of one kernel since the last reset."""
+    ms, n = ctypes.c_double(), ctypes.c_longlong()
+    st = _lib.attn_profile_read(int(kernel_id), ctypes.byref(ms), ctypes.byref(n))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_profile_read")
+    return ms.value, n.value
+
+
+def attn_bwd_noalloc(dout, qkv, out, lse, dqkv, B, T, C, NH, causal, dtype, stream=None,
+                     check=True) -> int:
+    """attn_bwd without a workspace argument: for callers that cannot allocate
+    device memory; the library's fixed scratch array is used instead."""
+    st = _lib.attn_bwd_noalloc(_ptr(dout), _ptr(qkv), _ptr(out), _ptr(lse), _ptr(dqkv), B, T, C, NH,
+                               int(causal), _dtype(dtype), _stream(stream))
+    if check and st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_noalloc")
+    return st

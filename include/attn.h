@@ -95,6 +95,47 @@ const char* attn_status_string(attn_status_t status);
  */
 attn_status_t attn_last_device_error(void* stream);
 
+/*
+ * Backward without a caller-provided workspace. No counterpart in the paper.
+ *
+ * For callers that cannot allocate device memory themselves: for example, a
+ * plug-in whose host framework owns every device allocation and hands over
+ * only the input and output buffers, or a latency-critical loop that must not
+ * call cudaMalloc (which can synchronise the device) after start-up.
+ * Same arguments and result as attn_bwd, minus the workspace. The scratch
+ * attn_bwd needs lives instead in a fixed array inside the library's own
+ * device memory, ATTN_NOALLOC_SCRATCH_BYTES per GPU that loads the library,
+ * held until the process exits. This call allocates nothing.
+ *   - Returns ATTN_ERR_WORKSPACE when attn_bwd_workspace_size(...) exceeds
+ *     ATTN_NOALLOC_SCRATCH_BYTES (roughly B*T*C*4 + B*NH*T*4 bytes must fit).
+ *   - The first call on each device looks up the array's device address;
+ *     make that first call before any stream capture.
+ *   - Every call shares the one array (the previous call's contents remain,
+ *     and each call re-initialises what must start at zero). Calls whose GPU
+ *     work overlaps, on different streams or from different host threads,
+ *     race on it: issue them in order on one stream.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+attn_status_t attn_bwd_noalloc(const void* dout, const void* qkv, const void* out, const float* lse,
+                               void* dqkv, int B, int T, int C, int NH, int causal,
+                               attn_dtype_t dtype, void* stream);
+
+/*
+ * Per-kernel timing (diagnostics; no counterpart on the pages beyond llm.c's
+ * benchmark timing loop). While enabled, every kernel the library launches is
+ * bracketed by two CUDA events recorded on its stream; attn_profile_read
+ * synchronises those events and returns the accumulated device time (ms) and
+ * launch count of one kernel since the last reset. Kernel ids:
+ *   0 forward, 1 backward pre-pass (D, zero dq accumulator),
+ *   2 backward main kernel, 3 backward dq conversion.
+ * Enabling adds two event records per launch; leave it off for timing runs.
+ * Not thread-safe with concurrent attn_fwd/attn_bwd calls from other threads.
+ */
+#define ATTN_PROFILE_NUM_KERNELS 4
+attn_status_t attn_profile_enable(int enable);
+attn_status_t attn_profile_reset(void);
+attn_status_t attn_profile_read(int kernel_id, double* total_ms, long long* launches);
+
 #ifdef __cplusplus
 }
 #endif
