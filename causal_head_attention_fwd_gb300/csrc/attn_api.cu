@@ -4,6 +4,7 @@
 #include <cstring>
 #include <cmath>
 #include <mutex>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -38,6 +39,61 @@ int* device_error_word() {
     g_error_addr[dev] = static_cast<int*>(p);
   }
   return g_error_addr[dev];
+}
+
+// ---------------------------------------------------------------- profiling
+struct ProfState {
+  bool enabled = false;
+  struct Pending { cudaEvent_t a, b; };
+  std::vector<Pending> pending[K_COUNT];
+  std::vector<cudaEvent_t> pool;
+  double total_ms[K_COUNT] = {0, 0, 0, 0};
+  long long count[K_COUNT] = {0, 0, 0, 0};
+  cudaEvent_t cur_begin[K_COUNT] = {nullptr, nullptr, nullptr, nullptr};
+};
+static ProfState g_prof;
+
+static cudaEvent_t take_event() {
+  if (!g_prof.pool.empty()) {
+    cudaEvent_t e = g_prof.pool.back();
+    g_prof.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+void profile_begin(KernelId k, cudaStream_t s) {
+  if (!g_prof.enabled) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  cudaEvent_t e = take_event();
+  if (e && cudaEventRecord(e, s) == cudaSuccess) g_prof.cur_begin[k] = e;
+}
+
+void profile_end(KernelId k, cudaStream_t s) {
+  if (!g_prof.enabled) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  cudaEvent_t a = g_prof.cur_begin[k];
+  g_prof.cur_begin[k] = nullptr;
+  if (!a) return;
+  cudaEvent_t b = take_event();
+  if (b && cudaEventRecord(b, s) == cudaSuccess) g_prof.pending[k].push_back({a, b});
+}
+
+// Resolve every pending event pair of kernel k into the running totals.
+static bool profile_drain(int k) {
+  for (auto& pe : g_prof.pending[k]) {
+    if (cudaEventSynchronize(pe.b) != cudaSuccess) return false;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, pe.a, pe.b) != cudaSuccess) return false;
+    g_prof.total_ms[k] += ms;
+    g_prof.count[k] += 1;
+    g_prof.pool.push_back(pe.a);
+    g_prof.pool.push_back(pe.b);
+  }
+  g_prof.pending[k].clear();
+  return true;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -183,4 +239,29 @@ extern "C" attn_status_t attn_last_device_error(void* stream) {
       return ATTN_ERR_CUDA;
   }
   return v == 0 ? ATTN_OK : (v == ATTN_ERR_TIMEOUT ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA);
+}
+
+extern "C" attn_status_t attn_profile_enable(int enable) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_prof.enabled = enable != 0;
+  return ATTN_OK;
+}
+
+extern "C" attn_status_t attn_profile_reset(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int k = 0; k < K_COUNT; ++k) {
+    if (!profile_drain(k)) return ATTN_ERR_CUDA;
+    g_prof.total_ms[k] = 0;
+    g_prof.count[k] = 0;
+  }
+  return ATTN_OK;
+}
+
+extern "C" attn_status_t attn_profile_read(int kernel_id, double* total_ms, long long* launches) {
+  if (kernel_id < 0 || kernel_id >= K_COUNT || !total_ms || !launches) return ATTN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!profile_drain(kernel_id)) return ATTN_ERR_CUDA;
+  *total_ms = g_prof.total_ms[kernel_id];
+  *launches = g_prof.count[kernel_id];
+  return ATTN_OK;
 }

@@ -401,6 +401,7 @@ static cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& md,
   auto k = attn_bwd_kernel<HS, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<HS>::ALLOC);
   if (e != cudaSuccess) return e;
+  ProfileScope ps(K_BWD_MAIN, stream);
   k<<<grid, BWD_THREADS, BwdSmem<HS>::ALLOC, stream>>>(mq, md, mg, p);
   return cudaGetLastError();
 }
@@ -412,6 +413,9 @@ cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_d
   const long long n_vec = (long long)pr.B * pr.T * pr.C / 8;
   const int threads = 256;
   const long long blocks = (n_vec + threads - 1) / threads;
+  cudaError_t e;
+  {
+  ProfileScope ps(K_BWD_PRE, stream);
   if (pr.hs == 64)
     attn_bwd_pre<64><<<(unsigned)blocks, threads, 0, stream>>>(
         static_cast<const uint4*>(dout), static_cast<const uint4*>(out), ws_D,
@@ -420,7 +424,8 @@ cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_d
     attn_bwd_pre<32><<<(unsigned)blocks, threads, 0, stream>>>(
         static_cast<const uint4*>(dout), static_cast<const uint4*>(out), ws_D,
         reinterpret_cast<float4*>(ws_dq), pr.T, pr.C, pr.NH, n_vec);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
 
   BwdParams p;
@@ -444,6 +449,7 @@ cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_d
                   : launch_bwd_main<32, false>(map_qkv, map_dout, map_dqkv, p, grid, stream);
   if (e != cudaSuccess) return e;
 
+  ProfileScope ps(K_BWD_DQ, stream);
   attn_bwd_dq_out<<<(unsigned)blocks, threads, 0, stream>>>(reinterpret_cast<const float4*>(ws_dq),
                                                             static_cast<uint4*>(dqkv), pr.C, n_vec);
   return cudaGetLastError();

@@ -314,6 +314,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mo, co
   auto k = attn_fwd_kernel<HS, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdSmem<HS>::ALLOC);
   if (e != cudaSuccess) return e;
+  ProfileScope ps(K_FWD, stream);
   k<<<grid, FWD_THREADS, FwdSmem<HS>::ALLOC, stream>>>(mq, mo, p);
   return cudaGetLastError();
 }

@@ -41,4 +41,16 @@ struct Problem {
 // attn_status_t code written by a kernel whose bounded wait gave up).
 int* device_error_word();
 
+// Optional per-kernel timing (see attn_profile_enable in include/attn.h).
+enum KernelId { K_FWD = 0, K_BWD_PRE = 1, K_BWD_MAIN = 2, K_BWD_DQ = 3, K_COUNT = 4 };
+void profile_begin(KernelId k, cudaStream_t s);
+void profile_end(KernelId k, cudaStream_t s);
+
+struct ProfileScope {
+  KernelId k;
+  cudaStream_t s;
+  ProfileScope(KernelId k_, cudaStream_t s_) : k(k_), s(s_) { profile_begin(k, s); }
+  ~ProfileScope() { profile_end(k, s); }
+};
+
 }  // namespace attn

@@ -35,6 +35,18 @@ __device__ __forceinline__ uint32_t lane_id() {
   return l;
 }
 
+// Per-warpgroup register budget change (all four warps of the warpgroup must
+// execute it). The increases of some warpgroups must be covered by the
+// decreases of others: the block's pool is its launch threads x registers.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(N));
+}
+
 // Named barrier over `nthreads` threads (multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
