@@ -19,8 +19,8 @@ namespace attn {
 cudaError_t launch_fwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_out, float* lse,
                             const Problem& pr, cudaStream_t stream);
 cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_dout,
-                            const CUtensorMap& map_dqkv, const void* dout, const void* out,
-                            const float* lse, void* dqkv, float* ws_D, float* ws_dq,
+                            const CUtensorMap& map_dqkv, const CUtensorMap& map_dqacc, const void* dout,
+                            const void* out, const float* lse, void* dqkv, float* ws_D, float* ws_dq,
                             const Problem& pr, cudaStream_t stream);
 
 static __device__ int g_error_word = 0;
@@ -220,7 +220,11 @@ extern "C" attn_status_t attn_bwd(const void* dout, const void* qkv, const void*
   float* ws_D = static_cast<float*>(workspace);
   float* ws_dq = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                           ((((size_t)B * NH * T * 4) + 255) & ~(size_t)255));
-  cudaError_t ce = launch_bwd_bf16(mq, md, mg, dout, out, lse, dqkv, ws_D, ws_dq, pr,
+  // fp32 dq accumulator (B, T, C): 32-column boxes (128 bytes) for the 128-byte swizzle
+  CUtensorMap ma;
+  if (!encode_3d(&ma, ws_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, T, B, 32, BM, CU_TENSOR_MAP_SWIZZLE_128B))
+    return ATTN_ERR_CUDA;
+  cudaError_t ce = launch_bwd_bf16(mq, md, mg, ma, dout, out, lse, dqkv, ws_D, ws_dq, pr,
                                    static_cast<cudaStream_t>(stream));
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

@@ -15,24 +15,33 @@
 // Three launches on the caller's stream:
 //   1. attn_bwd_pre:    D (fp32, (B,NH,T)) and zero the fp32 dq accumulator (B,T,C)
 //   2. attn_bwd_kernel: one CTA per (b, h, 128-key tile), looping over the query
-//      tiles that see those keys; S^T, dP^T, dV, dK, dQ on tcgen05, dQ reduced
-//      into the accumulator with vector atomics, dK/dV stored with TMA.
+//      tiles that see those keys; S^T, dP^T, dV, dK, dQ on tcgen05; dQ tiles are
+//      added into the accumulator with TMA bulk reductions; dK/dV stored by TMA.
 //   3. attn_bwd_dq_out: dq accumulator -> bf16 into dqkv[:, :, 0:C].
 //
-// Main kernel roles (10 warps):
-//   warps 0-3  P/dS warpgroup, thread = key row (TMEM lane); dK/dV epilogue
-//   warps 4-7  dQ warpgroup, thread = query row; TMEM -> atomics
-//   warp  8    loader: K, V once; Q, dO, lse, D per query tile (2 stages)
-//   warp  9    MMA issuer
+// Main kernel: 16 warps.
+//   warps 0-3   softmax warpgroup A: query columns [0, 64) of S^T/dP^T, thread = key row
+//   warps 4-7   softmax warpgroup B: query columns [64, 128)
+//   warps 8-11  dQ warpgroup: thread = query row; TMEM -> smem -> TMA reduce-add;
+//               at the end the dK/dV epilogue (thread = key row)
+//   warp  12    loader: K, V once; Q, dO, lse, D per query tile (3-stage ring)
+//   warp  13    MMA issuer; warps 14-15 idle
+// The softmax warpgroups copy S^T/dP^T of tile i into registers and release
+// them at once, so the tensor core computes S^T/dP^T of tile i+1 while P/dS of
+// tile i are formed. MMA order per step: S(i), dP(i), dV(i-1), dK(i-1), dQ(i-1).
 // TMEM columns: S^T [0,128) dP^T [128,256) P^T [256,320) dV [320,384)
 //               dK [384,448) dQ [448,512)
 #include "common.cuh"
 
 namespace attn {
 
-constexpr int BWD_STAGES = 2;
-constexpr int BWD_THREADS = 320;
+constexpr int BWD_STAGES = 3;
+constexpr int BWD_THREADS = 512;
 constexpr uint32_t TB_S = 0, TB_DP = 128, TB_P = 256, TB_DV = 320, TB_DK = 384, TB_DQ = 448;
+// register split: 2 softmax warpgroups up, the other 2 warpgroups down.
+// pool = 512 threads x 128 registers = 65536 = 256 x 168 + 256 x 88.
+constexpr uint32_t REG_SOFTMAX = 168, REG_OTHER = 88;
+static_assert(256 * REG_SOFTMAX + 256 * REG_OTHER <= 512 * 128, "register split exceeds the pool");
 
 template <int HS>
 struct BwdSmem {
@@ -41,9 +50,11 @@ struct BwdSmem {
   static constexpr int V_OFF = K_OFF + TILE;
   static constexpr int Q_OFF = V_OFF + TILE;                   // BWD_STAGES tiles
   static constexpr int DO_OFF = Q_OFF + BWD_STAGES * TILE;     // BWD_STAGES tiles
-  static constexpr int DS_OFF = DO_OFF + BWD_STAGES * TILE;    // dS^T: 2 blocks of [128 keys][64 q]
+  static constexpr int DS_OFF = DO_OFF + BWD_STAGES * TILE;    // dS^T: 2 blocks of [128 keys][64 q] bf16
   static constexpr int DS_BYTES = 2 * 128 * 128;
-  static constexpr int ROWST_OFF = DS_OFF + DS_BYTES;          // per stage: lse2[128], D[128]
+  static constexpr int DQ_OFF = DS_OFF + DS_BYTES;             // dQ fp32: HS/32 blocks of [128 q][32] SW128
+  static constexpr int DQ_BYTES = (HS / 32) * 128 * 128;
+  static constexpr int ROWST_OFF = DQ_OFF + DQ_BYTES;          // per stage: -lse*log2e [128], D [128]
   static constexpr int BYTES = ROWST_OFF + BWD_STAGES * 2 * 128 * 4;
   static constexpr int ALLOC = BYTES + 1024;
 };
@@ -51,7 +62,6 @@ struct BwdSmem {
 struct BwdParams {
   const float* lse;   // (B, NH, T)
   const float* D;     // (B, NH, T)
-  float* dq_acc;      // (B, T, C) fp32
   int* err;
   int T, NH, C;
   int n_kv;           // key tiles per head
@@ -117,19 +127,59 @@ __global__ void attn_bwd_dq_out(const float4* __restrict__ dq_acc, uint4* __rest
 }
 
 // ----------------------------------------------------------------------------
+// P^T and dS^T of 64 query columns for one key row (packed fp32 pair math):
+//   P  = exp2(s*c - lse*log2 e),   dS = P * (dP - D)
+// rs holds -lse*log2(e) for the 128 queries of the tile, then D. With MASK,
+// queries before the key (causal diagonal tile) and keys past T give 0.
+// ----------------------------------------------------------------------------
+template <bool MASK>
+__device__ __forceinline__ void bwd_p_ds(const uint32_t (&sv)[2][32], const uint32_t (&dpv)[2][32],
+                                         const float* rs, float c, int q0, int r, bool diag, bool key_ok,
+                                         uint32_t (&pk)[32], uint32_t (&dk)[32]) {
+  const float2 c2 = make_float2(c, c);
+#pragma unroll
+  for (int cq = 0; cq < 2; ++cq) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      const float4 l4 = *reinterpret_cast<const float4*>(rs + cq * 32 + i);
+      const float4 d4 = *reinterpret_cast<const float4*>(rs + 128 + cq * 32 + i);
+#pragma unroll
+      for (int u = 0; u < 4; u += 2) {
+        const float2 nl = u == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
+        const float2 dd = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
+        const float2 s2 = make_float2(__uint_as_float(sv[cq][i + u]), __uint_as_float(sv[cq][i + u + 1]));
+        const float2 dp2 = make_float2(__uint_as_float(dpv[cq][i + u]), __uint_as_float(dpv[cq][i + u + 1]));
+        const float2 x = fma2(s2, c2, nl);
+        float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        if (MASK) {
+          const int qq = q0 + cq * 32 + i + u;       // query index in the tile
+          if (!key_ok || (diag && qq < r)) e.x = 0.f;
+          if (!key_ok || (diag && qq + 1 < r)) e.y = 0.f;
+        }
+        const float2 ds = mul2(e, sub2(dp2, dd));
+        pk[cq * 16 + (i + u) / 2] = pack_bf16x2(e.x, e.y);
+        dk[cq * 16 + (i + u) / 2] = pack_bf16x2(ds.x, ds.y);
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
 // 2. main kernel
 // ----------------------------------------------------------------------------
 template <int HS, bool CAUSAL>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_dout,
-                const __grid_constant__ CUtensorMap map_dqkv, const BwdParams p) {
+                const __grid_constant__ CUtensorMap map_dqkv, const __grid_constant__ CUtensorMap map_dqacc,
+                const BwdParams p) {
   using G = TileGeom<HS>;
   using L = BwdSmem<HS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   __shared__ uint64_t bar_kv, bar_q_full[BWD_STAGES], bar_q_empty[BWD_STAGES];
-  __shared__ uint64_t bar_sdp, bar_p, bar_ds_free, bar_dq_full, bar_dq_free, bar_done;
+  __shared__ uint64_t bar_sdp_full, bar_sdp_free, bar_pds_full, bar_pds_free, bar_dq_full, bar_dq_free,
+      bar_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
 
@@ -150,9 +200,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
       mbar_init(&bar_q_full[s], 1);
       mbar_init(&bar_q_empty[s], 1);
     }
-    mbar_init(&bar_sdp, 1);
-    mbar_init(&bar_p, 128);
-    mbar_init(&bar_ds_free, 1);
+    mbar_init(&bar_sdp_full, 1);
+    mbar_init(&bar_sdp_free, 256);
+    mbar_init(&bar_pds_full, 256);
+    mbar_init(&bar_pds_free, 1);
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_free, 128);
     mbar_init(&bar_done, 1);
@@ -168,219 +219,254 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
   const uint32_t tmem = tmem_base_sh;
   int* gerr = p.err;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ loader
-    if (lane == 0) {
-      tma_prefetch_desc(&map_qkv);
-      tma_prefetch_desc(&map_dout);
-      mbar_arrive_expect_tx(&bar_kv, 2 * G::TILE_BYTES);
-      tma_load_3d(smem + L::K_OFF, &map_qkv, &bar_kv, p.C + h * HS, kv * BN, b);
-      tma_load_3d(smem + L::V_OFF, &map_qkv, &bar_kv, 2 * p.C + h * HS, kv * BN, b);
-    }
-    const float log2e = 1.4426950408889634f;
-    for (int it = 0; it < n_it; ++it) {
-      const int st = it % BWD_STAGES;
-      const int qi = i0 + it;
-      bool ok = true;
-      if (it >= BWD_STAGES) ok = mbar_wait(&bar_q_empty[st], ((it / BWD_STAGES) - 1) & 1, &abort_sh, gerr);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
+  if (warp >= 8) {
+    setmaxnreg_dec<REG_OTHER>();
+    if (warp == 12) {
+      // ------------------------------------------------------------ loader
       if (lane == 0) {
-        mbar_expect_tx(&bar_q_full[st], 2 * G::TILE_BYTES);
-        tma_load_3d(smem + L::Q_OFF + st * G::TILE_BYTES, &map_qkv, &bar_q_full[st], h * HS, qi * BM, b);
-        tma_load_3d(smem + L::DO_OFF + st * G::TILE_BYTES, &map_dout, &bar_q_full[st], h * HS, qi * BM, b);
+        tma_prefetch_desc(&map_qkv);
+        tma_prefetch_desc(&map_dout);
+        mbar_arrive_expect_tx(&bar_kv, 2 * G::TILE_BYTES);
+        tma_load_3d(smem + L::K_OFF, &map_qkv, &bar_kv, p.C + h * HS, kv * BN, b);
+        tma_load_3d(smem + L::V_OFF, &map_qkv, &bar_kv, 2 * p.C + h * HS, kv * BN, b);
       }
-      float* rs = reinterpret_cast<float*>(smem + L::ROWST_OFF) + st * 256;
+      // per query tile: -lse*log2(e) and D of its 128 rows, loaded into registers
+      // one tile ahead so their latency hides behind the ring wait
+      const float nlog2e = -1.4426950408889634f;
       const size_t rowbase = (size_t)bh * T;
+      float lv[4], dv[4];
+      auto load_rows = [&](int qi) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int qq = lane + 32 * k;
-        const int q = qi * BM + qq;
-        // rows past T: lse = +inf makes P = 0 there, D = 0
-        rs[qq] = q < T ? p.lse[rowbase + q] * log2e : INFINITY;
-        rs[128 + qq] = q < T ? p.D[rowbase + q] : 0.f;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_q_full[st]);
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_sq = make_idesc_bf16(BN, BM, false, false);   // [keys x q], K = HS
-      constexpr uint32_t id_kv = make_idesc_bf16(BN, HS, false, true);    // [keys x HS], K = q, B MN-major
-      constexpr uint32_t id_dq = make_idesc_bf16(BM, HS, true, true);     // [q x HS], K = keys, A,B MN-major
-      const uint32_t sK = smem_u32(smem + L::K_OFF), sV = smem_u32(smem + L::V_OFF);
-      const uint32_t sQ = smem_u32(smem + L::Q_OFF), sDO = smem_u32(smem + L::DO_OFF);
-      const uint32_t sDS = smem_u32(smem + L::DS_OFF);
-      bool ok = mbar_wait(&bar_kv, 0, &abort_sh, gerr);
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int st = it % BWD_STAGES;
-        if (!(ok = mbar_wait(&bar_q_full[st], (it / BWD_STAGES) & 1, &abort_sh, gerr))) break;
-        tc_fence_after();
-        const uint32_t q_a = sQ + st * G::TILE_BYTES, do_a = sDO + st * G::TILE_BYTES;
-        // S^T = K Q^T ; dP^T = V dO^T   (K-dim = HS)
-#pragma unroll
-        for (int k = 0; k < HS / 16; ++k)
-          mma_ss(tmem + TB_S, make_sdesc(sK + k * 32, 16, G::ATOM_BYTES, G::SWZ),
-                 make_sdesc(q_a + k * 32, 16, G::ATOM_BYTES, G::SWZ), id_sq, k > 0);
-#pragma unroll
-        for (int k = 0; k < HS / 16; ++k)
-          mma_ss(tmem + TB_DP, make_sdesc(sV + k * 32, 16, G::ATOM_BYTES, G::SWZ),
-                 make_sdesc(do_a + k * 32, 16, G::ATOM_BYTES, G::SWZ), id_sq, k > 0);
-        mma_commit(&bar_sdp);
-        if (!(ok = mbar_wait(&bar_p, it & 1, &abort_sh, gerr))) break;
-        tc_fence_after();
-        // dV += P^T dO  (A = P^T in TMEM, B = dO MN-major; K = 128 queries)
-#pragma unroll
-        for (int k = 0; k < BM / 16; ++k)
-          mma_ts(tmem + TB_DV, tmem + TB_P + k * 8,
-                 make_sdesc(do_a + k * 16 * G::ROW_BYTES, 16, G::ATOM_BYTES, G::SWZ), id_kv,
-                 (it > 0 || k > 0) ? 1u : 0u);
-        // dK += dS^T Q  (A = dS^T K-major: 2 blocks of 64 queries, B = Q MN-major)
-#pragma unroll
-        for (int k = 0; k < BM / 16; ++k)
-          mma_ss(tmem + TB_DK, make_sdesc(sDS + (k / 4) * 16384 + (k % 4) * 32, 16, 1024, SWZ_128B),
-                 make_sdesc(q_a + k * 16 * G::ROW_BYTES, 16, G::ATOM_BYTES, G::SWZ), id_kv,
-                 (it > 0 || k > 0) ? 1u : 0u);
-        if (it > 0) {
-          if (!(ok = mbar_wait(&bar_dq_free, (it - 1) & 1, &abort_sh, gerr))) break;
-          tc_fence_after();
+        for (int k = 0; k < 4; ++k) {
+          const int q = qi * BM + lane + 32 * k;
+          // rows past T: -lse2 = -inf makes P = 0 there, D = 0
+          lv[k] = q < T ? __ldg(p.lse + rowbase + q) * nlog2e : -INFINITY;
+          dv[k] = q < T ? __ldg(p.D + rowbase + q) : 0.f;
         }
-        // dQ = dS K  (A = dS: MN-major view of the dS^T tile, B = K MN-major; K-dim = 128 keys)
+      };
+      load_rows(i0);
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it % BWD_STAGES;
+        const int qi = i0 + it;
+        bool ok = true;
+        if (it >= BWD_STAGES) ok = mbar_wait(&bar_q_empty[st], ((it / BWD_STAGES) - 1) & 1, &abort_sh, gerr);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_expect_tx(&bar_q_full[st], 2 * G::TILE_BYTES);
+          tma_load_3d(smem + L::Q_OFF + st * G::TILE_BYTES, &map_qkv, &bar_q_full[st], h * HS, qi * BM, b);
+          tma_load_3d(smem + L::DO_OFF + st * G::TILE_BYTES, &map_dout, &bar_q_full[st], h * HS, qi * BM, b);
+        }
+        float* rs = reinterpret_cast<float*>(smem + L::ROWST_OFF) + st * 256;
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-          mma_ss(tmem + TB_DQ, make_sdesc(sDS + k * 16 * 128, 16384, 1024, SWZ_128B),
-                 make_sdesc(sK + k * 16 * G::ROW_BYTES, 16, G::ATOM_BYTES, G::SWZ), id_dq, k > 0);
-        mma_commit(&bar_dq_full);
-        // only commits that someone waits for (no arrival after the CTA retires)
-        if (it + 1 < n_it) mma_commit(&bar_ds_free);
-        if (it + BWD_STAGES < n_it) mma_commit(&bar_q_empty[st]);
+        for (int k = 0; k < 4; ++k) {
+          rs[lane + 32 * k] = lv[k];
+          rs[128 + lane + 32 * k] = dv[k];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_q_full[st]);
+        if (it + 1 < n_it) load_rows(qi + 1);
       }
-      if (ok) mma_commit(&bar_done);
+    } else if (warp == 13) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t id_sq = make_idesc_bf16(BN, BM, false, false);   // [keys x q], K = HS
+        constexpr uint32_t id_kv = make_idesc_bf16(BN, HS, false, true);    // [keys x HS], K = q, B MN-major
+        constexpr uint32_t id_dq = make_idesc_bf16(BM, HS, true, true);     // [q x HS], K = keys, A,B MN-major
+        const uint64_t dK0 = make_sdesc(smem_u32(smem + L::K_OFF), 16, G::ATOM_BYTES, G::SWZ);
+        const uint64_t dV0 = make_sdesc(smem_u32(smem + L::V_OFF), 16, G::ATOM_BYTES, G::SWZ);
+        const uint64_t dQ0 = make_sdesc(smem_u32(smem + L::Q_OFF), 16, G::ATOM_BYTES, G::SWZ);
+        const uint64_t dO0 = make_sdesc(smem_u32(smem + L::DO_OFF), 16, G::ATOM_BYTES, G::SWZ);
+        const uint64_t dSk = make_sdesc(smem_u32(smem + L::DS_OFF), 16, 1024, SWZ_128B);      // dS^T, K-major
+        const uint64_t dSm = make_sdesc(smem_u32(smem + L::DS_OFF), 16384, 1024, SWZ_128B);   // dS, MN-major
+        bool ok = mbar_wait(&bar_kv, 0, &abort_sh, gerr);
+        // dV, dK, dQ of query tile j (stage j % BWD_STAGES)
+        auto finish = [&](int j) -> bool {
+          const int sj = j % BWD_STAGES;
+          const uint64_t qd = desc_add(dQ0, sj * G::TILE_BYTES), od = desc_add(dO0, sj * G::TILE_BYTES);
+          if (!mbar_wait(&bar_pds_full, j & 1, &abort_sh, gerr)) return false;
+          tc_fence_after();
+          // dV += P^T dO  (A = P^T in TMEM, B = dO MN-major; K = 128 queries)
+#pragma unroll
+          for (int k = 0; k < BM / 16; ++k)
+            mma_ts(tmem + TB_DV, tmem + TB_P + k * 8, desc_add(od, k * 16 * G::ROW_BYTES), id_kv,
+                   (j > 0 || k > 0) ? 1u : 0u);
+          // dK += dS^T Q  (A = dS^T K-major: 2 blocks of 64 queries, B = Q MN-major)
+#pragma unroll
+          for (int k = 0; k < BM / 16; ++k)
+            mma_ss(tmem + TB_DK, desc_add(dSk, (k / 4) * 16384 + (k % 4) * 32),
+                   desc_add(qd, k * 16 * G::ROW_BYTES), id_kv, (j > 0 || k > 0) ? 1u : 0u);
+          if (j > 0) {
+            if (!mbar_wait(&bar_dq_free, (j - 1) & 1, &abort_sh, gerr)) return false;
+            tc_fence_after();
+          }
+          // dQ = dS K  (A = dS: MN-major view of the dS^T tile, B = K MN-major; K-dim = 128 keys)
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k)
+            mma_ss(tmem + TB_DQ, desc_add(dSm, k * 16 * 128), desc_add(dK0, k * 16 * G::ROW_BYTES), id_dq, k > 0);
+          mma_commit(&bar_dq_full);
+          // only commits that someone waits for (no arrival after the CTA retires)
+          if (j + 1 < n_it) mma_commit(&bar_pds_free);
+          if (j + BWD_STAGES < n_it) mma_commit(&bar_q_empty[sj]);
+          return true;
+        };
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int st = it % BWD_STAGES;
+          if (!(ok = mbar_wait(&bar_q_full[st], (it / BWD_STAGES) & 1, &abort_sh, gerr))) break;
+          if (it > 0 && !(ok = mbar_wait(&bar_sdp_free, (it - 1) & 1, &abort_sh, gerr))) break;
+          tc_fence_after();
+          const uint64_t qd = desc_add(dQ0, st * G::TILE_BYTES), od = desc_add(dO0, st * G::TILE_BYTES);
+          // S^T = K Q^T ; dP^T = V dO^T   (K-dim = HS)
+#pragma unroll
+          for (int k = 0; k < HS / 16; ++k)
+            mma_ss(tmem + TB_S, desc_add(dK0, k * 32), desc_add(qd, k * 32), id_sq, k > 0);
+#pragma unroll
+          for (int k = 0; k < HS / 16; ++k)
+            mma_ss(tmem + TB_DP, desc_add(dV0, k * 32), desc_add(od, k * 32), id_sq, k > 0);
+          mma_commit(&bar_sdp_full);
+          if (it > 0) ok = finish(it - 1);
+        }
+        if (ok) ok = finish(n_it - 1);
+        if (ok) mma_commit(&bar_done);
+      }
+    } else if (warp < 12) {
+      // ------------------------------------------------------------ dQ warpgroup
+      const int wq = warp - 8;
+      const int r = (wq << 5) + lane;                // query row (dQ) / key row (dK, dV)
+      const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+      const bool leader = (wq == 0 && lane == 0);
+      uint8_t* sdq = smem + L::DQ_OFF;
+      bool ok = true;
+      for (int it = 0; it < n_it; ++it) {
+        const int qi = i0 + it;
+        ok = mbar_wait(&bar_dq_full, it & 1, &abort_sh, gerr);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t a[HS / 32][32];
+#pragma unroll
+        for (int cc = 0; cc < HS / 32; ++cc) tmem_ld32(tmem + lane_off + TB_DQ + cc * 32, a[cc]);
+        tmem_ld_wait(a[0]);
+        if constexpr (HS == 64) tmem_tie32(a[HS / 32 - 1]);
+        tc_fence_before();
+        mbar_arrive(&bar_dq_free);
+        // the previous bulk reduction must have finished reading the staging tile
+        if (leader) bulk_wait_group_read0();
+        named_bar_sync(1, 128);
+        const float s = p.scale;
+#pragma unroll
+        for (int cc = 0; cc < HS / 32; ++cc) {
+          uint8_t* blk = sdq + cc * 16384;           // [128 q][32 fp32], 128-byte swizzle
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const float4 v = make_float4(__uint_as_float(a[cc][ch * 4 + 0]) * s, __uint_as_float(a[cc][ch * 4 + 1]) * s,
+                                         __uint_as_float(a[cc][ch * 4 + 2]) * s, __uint_as_float(a[cc][ch * 4 + 3]) * s);
+            *reinterpret_cast<float4*>(blk + swz_chunk_offset<64>(r, ch)) = v;
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader) {
+#pragma unroll
+          for (int cc = 0; cc < HS / 32; ++cc)
+            tma_reduce_add_3d(&map_dqacc, sdq + cc * 16384, h * HS + cc * 32, qi * BM, b);
+          bulk_commit_group();
+        }
+      }
+      if (leader) bulk_wait_group0();
+      // ---------------------------------------------------------- dK, dV epilogue
+      if (ok) {
+        ok = mbar_wait(&bar_done, 0, &abort_sh, gerr);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        tc_fence_after();
+        uint8_t* stage_v = smem + L::DS_OFF;         // dS^T tile is dead after the last MMA
+        uint8_t* stage_k = smem + L::DS_OFF + 16384;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t col = which == 0 ? TB_DV : TB_DK;
+          const float mul = which == 0 ? 1.f : p.scale;
+          uint8_t* stage = which == 0 ? stage_v : stage_k;
+#pragma unroll
+          for (int cc = 0; cc < HS; cc += 32) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_off + col + cc, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[ch * 8 + 0]) * mul, __uint_as_float(o[ch * 8 + 1]) * mul);
+              v.y = pack_bf16x2(__uint_as_float(o[ch * 8 + 2]) * mul, __uint_as_float(o[ch * 8 + 3]) * mul);
+              v.z = pack_bf16x2(__uint_as_float(o[ch * 8 + 4]) * mul, __uint_as_float(o[ch * 8 + 5]) * mul);
+              v.w = pack_bf16x2(__uint_as_float(o[ch * 8 + 6]) * mul, __uint_as_float(o[ch * 8 + 7]) * mul);
+              *reinterpret_cast<uint4*>(stage + swz_chunk_offset<HS>(r, cc / 8 + ch)) = v;
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader) {
+          tma_store_3d(&map_dqkv, stage_v, 2 * p.C + h * HS, kv * BN, b);
+          tma_store_3d(&map_dqkv, stage_k, p.C + h * HS, kv * BN, b);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+      }
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ P / dS warpgroup
-    const int r = (warp << 5) + lane;              // key row in the tile = TMEM lane
+  } else {
+    setmaxnreg_inc<REG_SOFTMAX>();
+    // ------------------------------------------------------------ softmax warpgroups
+    const int half = warp >> 2;                    // query columns [64*half, 64*half+64)
+    const int r = ((warp & 3) << 5) + lane;        // key row in the tile = TMEM lane
     const int key = kv * BN + r;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float c = p.scale_log2;
-    bool ok = true;
-    uint8_t* sds = smem + L::DS_OFF;
+    uint8_t* sds = smem + L::DS_OFF + half * 16384;
     for (int it = 0; it < n_it; ++it) {
       const int st = it % BWD_STAGES;
       const int qi = i0 + it;
-      ok = mbar_wait(&bar_q_full[st], (it / BWD_STAGES) & 1, &abort_sh, gerr);
-      ok = ok && mbar_wait(&bar_sdp, it & 1, &abort_sh, gerr);
-      if (ok && it > 0) ok = mbar_wait(&bar_ds_free, (it - 1) & 1, &abort_sh, gerr);
+      bool ok = mbar_wait(&bar_q_full[st], (it / BWD_STAGES) & 1, &abort_sh, gerr);
+      ok = ok && mbar_wait(&bar_sdp_full, it & 1, &abort_sh, gerr);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float* rs = reinterpret_cast<const float*>(smem + L::ROWST_OFF) + st * 256;
+      uint32_t sv[2][32], dpv[2][32];
+      tmem_ld32(tmem + lane_off + TB_S + half * 64, sv[0]);
+      tmem_ld32(tmem + lane_off + TB_S + half * 64 + 32, sv[1]);
+      tmem_ld32(tmem + lane_off + TB_DP + half * 64, dpv[0]);
+      tmem_ld32(tmem + lane_off + TB_DP + half * 64 + 32, dpv[1]);
+      tmem_ld_wait(sv[0]);
+      tmem_tie32(sv[1]);
+      tmem_tie32(dpv[0]);
+      tmem_tie32(dpv[1]);
+      tc_fence_before();
+      mbar_arrive(&bar_sdp_free);                  // S^T/dP^T columns may be overwritten now
+      const float* rs = reinterpret_cast<const float*>(smem + L::ROWST_OFF) + st * 256 + half * 64;
       const bool diag = CAUSAL && (qi == kv);
-      const bool key_ok = key < T;
-#pragma unroll 1
-      for (int cq = 0; cq < 4; ++cq) {
-        uint32_t sv[32], dpv[32];
-        tmem_ld32(tmem + lane_off + TB_S + cq * 32, sv);
-        tmem_ld32(tmem + lane_off + TB_DP + cq * 32, dpv);
-        tmem_ld_wait(sv);
-        tmem_tie32(dpv);
-        uint32_t pk[16];
-        uint32_t dk[16];
+      uint32_t pk[32], dk[32];
+      // masked variant only on the diagonal tile or a tile with keys past T
+      if (__any_sync(0xffffffffu, diag || key >= T))
+        bwd_p_ds<true>(sv, dpv, rs, c, half * 64, r, diag, key < T, pk, dk);
+      else
+        bwd_p_ds<false>(sv, dpv, rs, c, half * 64, r, false, true, pk, dk);
+      if (it > 0) {
+        ok = mbar_wait(&bar_pds_free, (it - 1) & 1, &abort_sh, gerr);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      tmem_st32(tmem + lane_off + TB_P + half * 32, pk);
+      // dS^T row `r`, queries [64*half, 64*half+64): block `half`, 8 chunks of 16 bytes
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float pp[2], dd[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qq = cq * 32 + i + u;
-            float e = ex2_approx(fmaf(__uint_as_float(sv[i + u]), c, -rs[qq]));
-            if (!key_ok || (diag && qq < r)) e = 0.f;
-            pp[u] = e;
-            dd[u] = e * (__uint_as_float(dpv[i + u]) - rs[128 + qq]);
-          }
-          pk[i / 2] = pack_bf16x2(pp[0], pp[1]);
-          dk[i / 2] = pack_bf16x2(dd[0], dd[1]);
-        }
-        tmem_st16(tmem + lane_off + TB_P + cq * 16, pk);
-        // dS^T row `r`, queries [32cq, 32cq+32): block cq/2, 16-byte chunks 4*(cq%2)..+3
-        uint8_t* blk = sds + (cq >> 1) * 16384;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint4 v = make_uint4(dk[ch * 4 + 0], dk[ch * 4 + 1], dk[ch * 4 + 2], dk[ch * 4 + 3]);
-          *reinterpret_cast<uint4*>(blk + swz_chunk_offset<64>(r, (cq & 1) * 4 + ch)) = v;
-        }
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 v = make_uint4(dk[ch * 4 + 0], dk[ch * 4 + 1], dk[ch * 4 + 2], dk[ch * 4 + 3]);
+        *reinterpret_cast<uint4*>(sds + swz_chunk_offset<64>(r, ch)) = v;
       }
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar_p);
-    }
-    // ---------------------------------------------------------- dK, dV epilogue
-    if (ok) {
-      ok = mbar_wait(&bar_done, 0, &abort_sh, gerr);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      tc_fence_after();
-      uint8_t* stage_v = sds;                // dS^T tile is dead after the last MMA
-      uint8_t* stage_k = sds + 16384;
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? TB_DV : TB_DK;
-        const float mul = which == 0 ? 1.f : p.scale;
-        uint8_t* stage = which == 0 ? stage_v : stage_k;
-#pragma unroll
-        for (int cc = 0; cc < HS; cc += 32) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_off + col + cc, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[ch * 8 + 0]) * mul, __uint_as_float(o[ch * 8 + 1]) * mul);
-            v.y = pack_bf16x2(__uint_as_float(o[ch * 8 + 2]) * mul, __uint_as_float(o[ch * 8 + 3]) * mul);
-            v.z = pack_bf16x2(__uint_as_float(o[ch * 8 + 4]) * mul, __uint_as_float(o[ch * 8 + 5]) * mul);
-            v.w = pack_bf16x2(__uint_as_float(o[ch * 8 + 6]) * mul, __uint_as_float(o[ch * 8 + 7]) * mul);
-            *reinterpret_cast<uint4*>(stage + swz_chunk_offset<HS>(r, cc / 8 + ch)) = v;
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (warp == 0 && lane == 0) {
-        tma_store_3d(&map_dqkv, stage_v, 2 * p.C + h * HS, kv * BN, b);
-        tma_store_3d(&map_dqkv, stage_k, p.C + h * HS, kv * BN, b);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ dQ warpgroup
-    const int wq = warp - 4;
-    const int r = (wq << 5) + lane;                // query row in the tile
-    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    for (int it = 0; it < n_it; ++it) {
-      const int qi = i0 + it;
-      bool ok = mbar_wait(&bar_dq_full, it & 1, &abort_sh, gerr);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t a[HS];
-      tmem_ld32(tmem + lane_off + TB_DQ, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
-      if constexpr (HS == 64) tmem_ld32(tmem + lane_off + TB_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&a[32]));
-      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&a[0]));
-      if constexpr (HS == 64) tmem_tie32(*reinterpret_cast<uint32_t(*)[32]>(&a[32]));
-      tc_fence_before();
-      mbar_arrive(&bar_dq_free);
-      const int t = qi * BM + r;
-      if (t < T) {
-        float* dst = p.dq_acc + ((size_t)b * T + t) * p.C + h * HS;
-        const float s = p.scale;
-#pragma unroll
-        for (int i = 0; i < HS; i += 4)
-          red_add_v4(dst + i, __uint_as_float(a[i]) * s, __uint_as_float(a[i + 1]) * s,
-                     __uint_as_float(a[i + 2]) * s, __uint_as_float(a[i + 3]) * s);
-      }
+      mbar_arrive(&bar_pds_full);
     }
   }
 
@@ -397,41 +483,41 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
 // ----------------------------------------------------------------------------
 template <int HS, bool CAUSAL>
 static cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& md, const CUtensorMap& mg,
-                                   const BwdParams& p, int grid, cudaStream_t stream) {
+                                   const CUtensorMap& macc, const BwdParams& p, int grid,
+                                   cudaStream_t stream) {
   auto k = attn_bwd_kernel<HS, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<HS>::ALLOC);
   if (e != cudaSuccess) return e;
   ProfileScope ps(K_BWD_MAIN, stream);
-  k<<<grid, BWD_THREADS, BwdSmem<HS>::ALLOC, stream>>>(mq, md, mg, p);
+  k<<<grid, BWD_THREADS, BwdSmem<HS>::ALLOC, stream>>>(mq, md, mg, macc, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_dout,
-                            const CUtensorMap& map_dqkv, const void* dout, const void* out,
-                            const float* lse, void* dqkv, float* ws_D, float* ws_dq,
+                            const CUtensorMap& map_dqkv, const CUtensorMap& map_dqacc, const void* dout,
+                            const void* out, const float* lse, void* dqkv, float* ws_D, float* ws_dq,
                             const Problem& pr, cudaStream_t stream) {
   const long long n_vec = (long long)pr.B * pr.T * pr.C / 8;
   const int threads = 256;
   const long long blocks = (n_vec + threads - 1) / threads;
   cudaError_t e;
   {
-  ProfileScope ps(K_BWD_PRE, stream);
-  if (pr.hs == 64)
-    attn_bwd_pre<64><<<(unsigned)blocks, threads, 0, stream>>>(
-        static_cast<const uint4*>(dout), static_cast<const uint4*>(out), ws_D,
-        reinterpret_cast<float4*>(ws_dq), pr.T, pr.C, pr.NH, n_vec);
-  else
-    attn_bwd_pre<32><<<(unsigned)blocks, threads, 0, stream>>>(
-        static_cast<const uint4*>(dout), static_cast<const uint4*>(out), ws_D,
-        reinterpret_cast<float4*>(ws_dq), pr.T, pr.C, pr.NH, n_vec);
-  e = cudaGetLastError();
+    ProfileScope ps(K_BWD_PRE, stream);
+    if (pr.hs == 64)
+      attn_bwd_pre<64><<<(unsigned)blocks, threads, 0, stream>>>(
+          static_cast<const uint4*>(dout), static_cast<const uint4*>(out), ws_D,
+          reinterpret_cast<float4*>(ws_dq), pr.T, pr.C, pr.NH, n_vec);
+    else
+      attn_bwd_pre<32><<<(unsigned)blocks, threads, 0, stream>>>(
+          static_cast<const uint4*>(dout), static_cast<const uint4*>(out), ws_D,
+          reinterpret_cast<float4*>(ws_dq), pr.T, pr.C, pr.NH, n_vec);
+    e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;
 
   BwdParams p;
   p.lse = lse;
   p.D = ws_D;
-  p.dq_acc = ws_dq;
   p.err = device_error_word();
   p.T = pr.T;
   p.NH = pr.NH;
@@ -442,11 +528,11 @@ cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_d
   p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)pr.hs));
   const int grid = p.n_kv * p.BH;
   if (pr.hs == 64)
-    e = pr.causal ? launch_bwd_main<64, true>(map_qkv, map_dout, map_dqkv, p, grid, stream)
-                  : launch_bwd_main<64, false>(map_qkv, map_dout, map_dqkv, p, grid, stream);
+    e = pr.causal ? launch_bwd_main<64, true>(map_qkv, map_dout, map_dqkv, map_dqacc, p, grid, stream)
+                  : launch_bwd_main<64, false>(map_qkv, map_dout, map_dqkv, map_dqacc, p, grid, stream);
   else
-    e = pr.causal ? launch_bwd_main<32, true>(map_qkv, map_dout, map_dqkv, p, grid, stream)
-                  : launch_bwd_main<32, false>(map_qkv, map_dout, map_dqkv, p, grid, stream);
+    e = pr.causal ? launch_bwd_main<32, true>(map_qkv, map_dout, map_dqkv, map_dqacc, p, grid, stream)
+                  : launch_bwd_main<32, false>(map_qkv, map_dout, map_dqkv, map_dqacc, p, grid, stream);
   if (e != cudaSuccess) return e;
 
   ProfileScope ps(K_BWD_DQ, stream);

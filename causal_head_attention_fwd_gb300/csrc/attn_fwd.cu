@@ -55,7 +55,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   __shared__ uint64_t bar_q, bar_k_full[FWD_STAGES], bar_v_full[FWD_STAGES], bar_kv_empty[FWD_STAGES];
-  __shared__ uint64_t bar_s[2], bar_p[2], bar_o[2];
+  __shared__ uint64_t bar_s[2], bar_sfree[2], bar_p[2], bar_pv[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
 
@@ -87,8 +87,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_s[i], 1);
+      mbar_init(&bar_sfree[i], 128);
       mbar_init(&bar_p[i], 128);
-      mbar_init(&bar_o[i], 1);
+      mbar_init(&bar_pv[i], 1);
     }
     fence_mbar_init();
   }
@@ -127,58 +128,59 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc_bf16(BM, BN, false, false);
       constexpr uint32_t idesc_o = make_idesc_bf16(BM, HS, false, true);
-      const uint32_t sQ = smem_u32(smem + L::Q_OFF);
-      const uint32_t sK = smem_u32(smem + L::K_OFF);
-      const uint32_t sV = smem_u32(smem + L::V_OFF);
-      const uint32_t tS[2] = {tmem + TM_S0, tmem + TM_S1};
-      const uint32_t tO[2] = {tmem + TM_O0, tmem + TM_O1};
-      const uint32_t tP[2] = {tmem + TM_P0, tmem + TM_P1};
-      bool ok = mbar_wait(&bar_q, 0, &abort_sh, gerr);
+      const uint64_t dQ0 = make_sdesc(smem_u32(smem + L::Q_OFF), 16, G::ATOM_BYTES, G::SWZ);
+      const uint64_t dK0 = make_sdesc(smem_u32(smem + L::K_OFF), 16, G::ATOM_BYTES, G::SWZ);
+      const uint64_t dV0 = make_sdesc(smem_u32(smem + L::V_OFF), 16, G::ATOM_BYTES, G::SWZ);
       // S_i(j) = Q_i K_j^T : K = HS in steps of 16 (32 bytes inside the swizzle row)
       auto issue_s = [&](int i, int st) {
-        const uint32_t qa = sQ + i * G::TILE_BYTES, ka = sK + st * G::TILE_BYTES;
+        const uint64_t qd = desc_add(dQ0, i * G::TILE_BYTES), kd = desc_add(dK0, st * G::TILE_BYTES);
+        const uint32_t d = tmem + (i ? TM_S1 : TM_S0);
 #pragma unroll
-        for (int k = 0; k < HS / 16; ++k)
-          mma_ss(tS[i], make_sdesc(qa + k * 32, 16, G::ATOM_BYTES, G::SWZ),
-                 make_sdesc(ka + k * 32, 16, G::ATOM_BYTES, G::SWZ), idesc_s, k > 0);
+        for (int k = 0; k < HS / 16; ++k) mma_ss(d, desc_add(qd, k * 32), desc_add(kd, k * 32), idesc_s, k > 0);
+        mma_commit(&bar_s[i]);
       };
       // O_i += P_i V_j : K = 128 keys in steps of 16 (16 rows of V = 2 atoms)
       auto issue_pv = [&](int i, int st, bool acc) {
-        const uint32_t va = sV + st * G::TILE_BYTES;
+        const uint64_t vd = desc_add(dV0, st * G::TILE_BYTES);
+        const uint32_t d = tmem + (i ? TM_O1 : TM_O0), a = tmem + (i ? TM_P1 : TM_P0);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          mma_ts(tO[i], tP[i] + k * 8, make_sdesc(va + k * 16 * G::ROW_BYTES, 16, G::ATOM_BYTES, G::SWZ),
-                 idesc_o, (acc || k > 0) ? 1u : 0u);
+          mma_ts(d, a + k * 8, desc_add(vd, k * 16 * G::ROW_BYTES), idesc_o, (acc || k > 0) ? 1u : 0u);
+        mma_commit(&bar_pv[i]);
       };
+      bool ok = mbar_wait(&bar_q, 0, &abort_sh, gerr) && mbar_wait(&bar_k_full[0], 0, &abort_sh, gerr);
+      if (ok) {
+        tc_fence_after();
+        for (int i = 0; i < 2; ++i)
+          if (n_tile[i] > 0) issue_s(i, 0);
+      }
+      // Per key tile j: S_i(j+1) for each query tile as soon as its softmax
+      // warps hold S_i(j) in registers, then O_i += P_i(j) V_j.
       for (int j = 0; ok && j < n_max; ++j) {
         const int st = j % FWD_STAGES;
-        const uint32_t ph = (j / FWD_STAGES) & 1;
-        if (j == 0) {
-          if (!(ok = mbar_wait(&bar_k_full[st], ph, &abort_sh, gerr))) break;
-          tc_fence_after();
-          for (int i = 0; i < 2; ++i)
-            if (n_tile[i] > 0) { issue_s(i, st); mma_commit(&bar_s[i]); }
-        }
-        if (!(ok = mbar_wait(&bar_v_full[st], ph, &abort_sh, gerr))) break;
         const int st1 = (j + 1) % FWD_STAGES;
-        const uint32_t ph1 = ((j + 1) / FWD_STAGES) & 1;
+        bool k_ready = false;
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (j + 1 >= n_tile[i]) continue;
+          if (!(ok = mbar_wait(&bar_sfree[i], j & 1, &abort_sh, gerr))) break;
+          if (!k_ready) {
+            if (!(ok = mbar_wait(&bar_k_full[st1], ((j + 1) / FWD_STAGES) & 1, &abort_sh, gerr))) break;
+            k_ready = true;
+          }
+          tc_fence_after();
+          issue_s(i, st1);
+        }
+        if (!ok) break;
+        if (!(ok = mbar_wait(&bar_v_full[st], (j / FWD_STAGES) & 1, &abort_sh, gerr))) break;
         for (int i = 0; i < 2 && ok; ++i) {
           if (j >= n_tile[i]) continue;
           if (!(ok = mbar_wait(&bar_p[i], j & 1, &abort_sh, gerr))) break;
           tc_fence_after();
           issue_pv(i, st, j > 0);
-          if (j + 1 < n_tile[i]) {
-            if (!(ok = mbar_wait(&bar_k_full[st1], ph1, &abort_sh, gerr))) break;
-            tc_fence_after();
-            issue_s(i, st1);
-            mma_commit(&bar_s[i]);
-          } else {
-            mma_commit(&bar_o[i]);
-          }
         }
         // release the K/V stage only if the producer will refill it (every
         // commit issued is awaited, so no arrival lands after the CTA retires)
-        if (j + FWD_STAGES < n_max) mma_commit(&bar_kv_empty[st]);
+        if (ok && j + FWD_STAGES < n_max) mma_commit(&bar_kv_empty[st]);
       }
     }
   } else {
@@ -195,8 +197,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      ok = mbar_wait(&bar_s[wg], j & 1, &abort_sh, gerr);
-      ok = __all_sync(0xffffffffu, ok);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[wg], j & 1, &abort_sh, gerr));
       if (!ok) break;
       tc_fence_after();
       uint32_t s[4][32];
@@ -208,59 +209,82 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
       tmem_tie32(s[1]);
       tmem_tie32(s[2]);
       tmem_tie32(s[3]);
+      tc_fence_before();
+      mbar_arrive(&bar_sfree[wg]);                     // S columns may be overwritten now
       // mask: causal diagonal tile (key > row), or keys past T (non-causal tail)
       const int kbase = j * BN;
       int limit = BN;                                  // keys [kbase, kbase+limit) are visible
       if (CAUSAL) { if (kbase + BN > t) limit = t - kbase + 1; }
       else { if (kbase + BN > T) limit = T - kbase; }
-      float mx = -INFINITY;
+      if (__any_sync(0xffffffffu, limit < BN)) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < 4; ++q)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float v = __uint_as_float(s[q][i]);
-          if (q * 32 + i >= limit) v = -INFINITY;
-          s[q][i] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
-        }
-      const float m_new = fmaxf(m_run, mx);
-      const float alpha = ex2_approx((m_run - m_new) * c);
-      const float mc = m_new * c;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[64];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float e0 = ex2_approx(fmaf(__uint_as_float(s[q][i]), c, -mc));
-          const float e1 = ex2_approx(fmaf(__uint_as_float(s[q][i + 1]), c, -mc));
-          ls[q] += e0 + e1;
-          pk[q * 16 + i / 2] = pack_bf16x2(e0, e1);
-        }
-      l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-      m_run = m_new;
-      tmem_st32(tP + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      // rescale the running output when this row's max moved (O is idle here:
-      // the previous P.V finished before S_j was signalled)
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int cc = 0; cc < HS; cc += 32) {
-          uint32_t o[32];
-          tmem_ld32(tO + cc, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + cc, o);
-        }
+          for (int i = 0; i < 32; ++i)
+            if (q * 32 + i >= limit) s[q][i] = __float_as_uint(-INFINITY);
       }
+      // row max: 3-input max in 8 independent chains, then a short tree
+      float mx8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int i = 0; i < 32; i += 2)
+          mx8[(i >> 1) & 7] = fmax3(mx8[(i >> 1) & 7], __uint_as_float(s[q][i]), __uint_as_float(s[q][i + 1]));
+      const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+      // Lazy rescaling: the exponent reference m_run only moves when the row
+      // max exceeds it by more than 8 (log2 units), so p <= 2^8 and O is
+      // rescaled rarely. Result and lse are exact for any reference value.
+      const float m_new = (mx - m_run) * c > 8.f ? mx : m_run;
+      const float alpha = ex2_approx((m_run - m_new) * c);
+      const float2 c2 = make_float2(c, c), nmc = make_float2(-m_new * c, -m_new * c);
+      float2 ls[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+      // p = exp2(s*c - m*c) in packed pairs; P goes to TMEM in two 64-key halves
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq)
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int q = hf * 2 + qq;
+            const float2 x = fma2(make_float2(__uint_as_float(s[q][i]), __uint_as_float(s[q][i + 1])), c2, nmc);
+            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            ls[(i >> 1) & 3] = add2(ls[(i >> 1) & 3], e);
+            pk[qq * 16 + i / 2] = pack_bf16x2(e.x, e.y);
+          }
+        if (hf == 0 && j > 0) {
+          // P_{j-1} must have been consumed (and O updated) by the previous P.V
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_pv[wg], (j - 1) & 1, &abort_sh, gerr));
+          if (!ok) break;
+          tc_fence_after();
+          // rescale the running output when this row's reference max moved
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int cc = 0; cc < HS; cc += 32) {
+              uint32_t o[32];
+              tmem_ld32(tO + cc, o);
+              tmem_ld_wait(o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tO + cc, o);
+            }
+          }
+        }
+        tmem_st32(tP + hf * 32, pk);
+      }
+      if (!ok) break;
+      const float lsum = ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
+      l_run = l_run * alpha + lsum;
+      m_run = m_new;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar_p[wg]);
     }
     // ---------------------------------------------------------- epilogue
     if (n > 0 && ok) {
-      ok = mbar_wait(&bar_o[wg], 0, &abort_sh, gerr);
+      ok = mbar_wait(&bar_pv[wg], (n - 1) & 1, &abort_sh, gerr);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (n > 0 && ok) {
