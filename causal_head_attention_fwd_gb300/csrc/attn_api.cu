@@ -41,6 +41,20 @@ int* device_error_word() {
   return g_error_addr[dev];
 }
 
+static int g_sm_count[kMaxDevices] = {0};
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sm_count[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
 // ---------------------------------------------------------------- profiling
 struct ProfState {
   bool enabled = false;
@@ -176,7 +190,7 @@ extern "C" attn_status_t attn_fwd(const void* qkv, void* out, float* lse, int B,
       overlaps(lse, (size_t)B * NH * T * 4, out, (size_t)B * T * C * e))
     return ATTN_ERR_INVALID_ARG;
   Problem pr{B, T, C, NH, C / NH, causal};
-  if (!device_error_word()) return ATTN_ERR_CUDA;
+  if (!device_error_word() || device_sm_count() <= 0) return ATTN_ERR_CUDA;
   const CUtensorMapSwizzle swz = pr.hs == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap mq, mo;
   if (!encode_3d(&mq, qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3 * C, T, B, pr.hs, BM, swz) ||
@@ -210,7 +224,7 @@ extern "C" attn_status_t attn_bwd(const void* dout, const void* qkv, const void*
       overlaps(dqkv, n3, lse, nl) || (workspace && overlaps(dqkv, n3, workspace, need)))
     return ATTN_ERR_INVALID_ARG;
   Problem pr{B, T, C, NH, C / NH, causal};
-  if (!device_error_word()) return ATTN_ERR_CUDA;
+  if (!device_error_word() || device_sm_count() <= 0) return ATTN_ERR_CUDA;
   const CUtensorMapSwizzle swz = pr.hs == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap mq, md, mg;
   if (!encode_3d(&mq, qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3 * C, T, B, pr.hs, BM, swz) ||

@@ -14,49 +14,54 @@
 //
 // Three launches on the caller's stream:
 //   1. attn_bwd_pre:    D (fp32, (B,NH,T)) and zero the fp32 dq accumulator (B,T,C)
-//   2. attn_bwd_kernel: one CTA per (b, h, 128-key tile), looping over the query
-//      tiles that see those keys; S^T, dP^T, dV, dK, dQ on tcgen05; dQ tiles are
-//      added into the accumulator with TMA bulk reductions; dK/dV stored by TMA.
+//   2. attn_bwd_kernel: persistent, one CTA per SM. Work item = (128-key tile,
+//      b, h); a CTA walks its items (heavy causal key tiles first, dealt in a
+//      snake order over the CTAs) and, per item, the query tiles that see
+//      those keys. S^T, dP^T, dV, dK, dQ on tcgen05; dQ tiles are added into
+//      the accumulator with TMA bulk reductions; dK/dV stored by TMA.
+//      K/V are double-buffered and the Q/dO ring runs on across items, so the
+//      next item's loads and the last item's dK/dV stores overlap compute.
 //   3. attn_bwd_dq_out: dq accumulator -> bf16 into dqkv[:, :, 0:C].
 //
 // Main kernel: 16 warps.
 //   warps 0-3   softmax warpgroup A: query columns [0, 64) of S^T/dP^T, thread = key row
 //   warps 4-7   softmax warpgroup B: query columns [64, 128)
 //   warps 8-11  dQ warpgroup: thread = query row; TMEM -> smem -> TMA reduce-add;
-//               at the end the dK/dV epilogue (thread = key row)
-//   warp  12    loader: K, V once; Q, dO, lse, D per query tile (3-stage ring)
+//               after each item the dK/dV epilogue (thread = key row)
+//   warp  12    loader: K, V per item; Q, dO, lse, D per query tile (2-stage ring)
 //   warp  13    MMA issuer; warps 14-15 idle
-// The softmax warpgroups copy S^T/dP^T of tile i into registers and release
-// them at once, so the tensor core computes S^T/dP^T of tile i+1 while P/dS of
-// tile i are formed. MMA order per step: S(i), dP(i), dV(i-1), dK(i-1), dQ(i-1).
+// The softmax warpgroups copy S^T/dP^T of step g into registers and release
+// them at once, so the tensor core computes S^T/dP^T of step g+1 while P/dS of
+// step g are formed. MMA order: S(g), dP(g), dV(g-1), dK(g-1), dQ(g-1).
 // TMEM columns: S^T [0,128) dP^T [128,256) P^T [256,320) dV [320,384)
 //               dK [384,448) dQ [448,512)
 #include "common.cuh"
 
 namespace attn {
 
-constexpr int BWD_STAGES = 3;
+constexpr int BWD_STAGES = 2;
 constexpr int BWD_THREADS = 512;
 constexpr uint32_t TB_S = 0, TB_DP = 128, TB_P = 256, TB_DV = 320, TB_DK = 384, TB_DQ = 448;
 // register split: 2 softmax warpgroups up, the other 2 warpgroups down.
-// pool = 512 threads x 128 registers = 65536 = 256 x 168 + 256 x 88.
-constexpr uint32_t REG_SOFTMAX = 168, REG_OTHER = 88;
+// pool = 512 threads x 128 registers = 65536 = 256 x 160 + 256 x 96.
+constexpr uint32_t REG_SOFTMAX = 160, REG_OTHER = 96;
 static_assert(256 * REG_SOFTMAX + 256 * REG_OTHER <= 512 * 128, "register split exceeds the pool");
 
 template <int HS>
 struct BwdSmem {
   static constexpr int TILE = TileGeom<HS>::TILE_BYTES;
-  static constexpr int K_OFF = 0;
-  static constexpr int V_OFF = K_OFF + TILE;
-  static constexpr int Q_OFF = V_OFF + TILE;                   // BWD_STAGES tiles
+  static constexpr int K_OFF = 0;                              // 2 buffers
+  static constexpr int V_OFF = K_OFF + 2 * TILE;               // 2 buffers
+  static constexpr int Q_OFF = V_OFF + 2 * TILE;               // BWD_STAGES tiles
   static constexpr int DO_OFF = Q_OFF + BWD_STAGES * TILE;     // BWD_STAGES tiles
   static constexpr int DS_OFF = DO_OFF + BWD_STAGES * TILE;    // dS^T: 2 blocks of [128 keys][64 q] bf16
   static constexpr int DS_BYTES = 2 * 128 * 128;
-  static constexpr int DQ_OFF = DS_OFF + DS_BYTES;             // dQ fp32: HS/32 blocks of [128 q][32] SW128
+  static constexpr int DQ_OFF = DS_OFF + DS_BYTES;             // dQ fp32 [128 q][32] SW128 blocks; dK/dV staging
   static constexpr int DQ_BYTES = (HS / 32) * 128 * 128;
   static constexpr int ROWST_OFF = DQ_OFF + DQ_BYTES;          // per stage: -lse*log2e [128], D [128]
   static constexpr int BYTES = ROWST_OFF + BWD_STAGES * 2 * 128 * 4;
   static constexpr int ALLOC = BYTES + 1024;
+  static_assert(2 * TILE <= DQ_BYTES, "dK/dV staging must fit in the dQ staging area");
 };
 
 struct BwdParams {
@@ -66,9 +71,33 @@ struct BwdParams {
   int T, NH, C;
   int n_kv;           // key tiles per head
   int BH;
+  int n_items;        // n_kv * BH work items
   float scale;        // 1/sqrt(hs)
   float scale_log2;   // scale * log2(e)
 };
+
+// Work item k of a CTA: rounds of gridDim.x items, snake order (even rounds
+// left to right, odd rounds right to left) so heavy and light items pair up.
+__device__ __forceinline__ int bwd_item(int k) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
+struct BwdItem {
+  int kv, bh, b, h, i0, n_it;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ BwdItem bwd_decode(int idx, const BwdParams& p) {
+  BwdItem it;
+  it.kv = idx / p.BH;                       // key tile; tile 0 (most causal work) first
+  it.bh = idx % p.BH;
+  it.b = it.bh / p.NH;
+  it.h = it.bh % p.NH;
+  it.i0 = CAUSAL ? it.kv : 0;               // first query tile that sees these keys
+  it.n_it = (p.T + BM - 1) / BM - it.i0;
+  return it;
+}
 
 // ----------------------------------------------------------------------------
 // 1. D = rowsum(dout * out) per head; zero the dq accumulator.
@@ -177,25 +206,30 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  __shared__ uint64_t bar_kv, bar_q_full[BWD_STAGES], bar_q_empty[BWD_STAGES];
+  __shared__ uint64_t bar_kv_full[2], bar_kv_empty[2], bar_q_full[BWD_STAGES], bar_q_empty[BWD_STAGES];
   __shared__ uint64_t bar_sdp_full, bar_sdp_free, bar_pds_full, bar_pds_free, bar_dq_full, bar_dq_free,
-      bar_done;
+      bar_done, bar_epi_free;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kv = (int)(blockIdx.x / p.BH);          // key tile; tile 0 has the most work
-  const int bh = blockIdx.x % p.BH;
-  const int b = bh / p.NH, h = bh % p.NH;
   const int T = p.T;
-  const int n_q_all = (T + BM - 1) / BM;
-  const int i0 = CAUSAL ? kv : 0;                   // first query tile that sees these keys
-  const int n_it = n_q_all - i0;
+  // this CTA's items and total number of steps (query tiles over all items)
+  int n_items_cta = 0, total_g = 0;
+  for (int k = 0;; ++k) {
+    const int idx = bwd_item(k);
+    if (idx >= p.n_items) break;
+    ++n_items_cta;
+    total_g += bwd_decode<CAUSAL>(idx, p).n_it;
+  }
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
-    mbar_init(&bar_kv, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_kv_full[s], 1);
+      mbar_init(&bar_kv_empty[s], 1);
+    }
     for (int s = 0; s < BWD_STAGES; ++s) {
       mbar_init(&bar_q_full[s], 1);
       mbar_init(&bar_q_empty[s], 1);
@@ -207,6 +241,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_free, 128);
     mbar_init(&bar_done, 1);
+    mbar_init(&bar_epi_free, 128);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -226,16 +261,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
       if (lane == 0) {
         tma_prefetch_desc(&map_qkv);
         tma_prefetch_desc(&map_dout);
-        mbar_arrive_expect_tx(&bar_kv, 2 * G::TILE_BYTES);
-        tma_load_3d(smem + L::K_OFF, &map_qkv, &bar_kv, p.C + h * HS, kv * BN, b);
-        tma_load_3d(smem + L::V_OFF, &map_qkv, &bar_kv, 2 * p.C + h * HS, kv * BN, b);
       }
       // per query tile: -lse*log2(e) and D of its 128 rows, loaded into registers
-      // one tile ahead so their latency hides behind the ring wait
+      // one step ahead so their latency hides behind the ring wait
       const float nlog2e = -1.4426950408889634f;
-      const size_t rowbase = (size_t)bh * T;
       float lv[4], dv[4];
-      auto load_rows = [&](int qi) {
+      auto load_rows = [&](int bh, int qi) {
+        const size_t rowbase = (size_t)bh * T;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int q = qi * BM + lane + 32 * k;
@@ -244,28 +276,49 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
           dv[k] = q < T ? __ldg(p.D + rowbase + q) : 0.f;
         }
       };
-      load_rows(i0);
-      for (int it = 0; it < n_it; ++it) {
-        const int st = it % BWD_STAGES;
-        const int qi = i0 + it;
-        bool ok = true;
-        if (it >= BWD_STAGES) ok = mbar_wait(&bar_q_empty[st], ((it / BWD_STAGES) - 1) & 1, &abort_sh, gerr);
-        ok = __all_sync(0xffffffffu, ok);
+      bool ok = true;
+      int g = 0;
+      if (n_items_cta > 0) {
+        const BwdItem f = bwd_decode<CAUSAL>(bwd_item(0), p);
+        load_rows(f.bh, f.i0);
+      }
+      for (int ic = 0; ok && ic < n_items_cta; ++ic) {
+        const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
+        const int kb = ic & 1;
+        if (ic >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&bar_kv_empty[kb], ((ic >> 1) - 1) & 1, &abort_sh, gerr));
         if (!ok) break;
         if (lane == 0) {
-          mbar_expect_tx(&bar_q_full[st], 2 * G::TILE_BYTES);
-          tma_load_3d(smem + L::Q_OFF + st * G::TILE_BYTES, &map_qkv, &bar_q_full[st], h * HS, qi * BM, b);
-          tma_load_3d(smem + L::DO_OFF + st * G::TILE_BYTES, &map_dout, &bar_q_full[st], h * HS, qi * BM, b);
+          mbar_arrive_expect_tx(&bar_kv_full[kb], 2 * G::TILE_BYTES);
+          tma_load_3d(smem + L::K_OFF + kb * G::TILE_BYTES, &map_qkv, &bar_kv_full[kb], p.C + w.h * HS, w.kv * BN, w.b);
+          tma_load_3d(smem + L::V_OFF + kb * G::TILE_BYTES, &map_qkv, &bar_kv_full[kb], 2 * p.C + w.h * HS, w.kv * BN, w.b);
         }
-        float* rs = reinterpret_cast<float*>(smem + L::ROWST_OFF) + st * 256;
+        for (int it = 0; it < w.n_it; ++it, ++g) {
+          const int st = g % BWD_STAGES;
+          const int qi = w.i0 + it;
+          if (g >= BWD_STAGES)
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar_q_empty[st], ((g / BWD_STAGES) - 1) & 1, &abort_sh, gerr));
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_expect_tx(&bar_q_full[st], 2 * G::TILE_BYTES);
+            tma_load_3d(smem + L::Q_OFF + st * G::TILE_BYTES, &map_qkv, &bar_q_full[st], w.h * HS, qi * BM, w.b);
+            tma_load_3d(smem + L::DO_OFF + st * G::TILE_BYTES, &map_dout, &bar_q_full[st], w.h * HS, qi * BM, w.b);
+          }
+          float* rs = reinterpret_cast<float*>(smem + L::ROWST_OFF) + st * 256;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          rs[lane + 32 * k] = lv[k];
-          rs[128 + lane + 32 * k] = dv[k];
+          for (int k = 0; k < 4; ++k) {
+            rs[lane + 32 * k] = lv[k];
+            rs[128 + lane + 32 * k] = dv[k];
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_q_full[st]);
+          // prefetch the rows of the next step (this item or the next one)
+          if (it + 1 < w.n_it) {
+            load_rows(w.bh, qi + 1);
+          } else if (ic + 1 < n_items_cta) {
+            const BwdItem nx = bwd_decode<CAUSAL>(bwd_item(ic + 1), p);
+            load_rows(nx.bh, nx.i0);
+          }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_q_full[st]);
-        if (it + 1 < n_it) load_rows(qi + 1);
       }
     } else if (warp == 13) {
       // ------------------------------------------------------------ MMA issuer
@@ -279,55 +332,73 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
         const uint64_t dO0 = make_sdesc(smem_u32(smem + L::DO_OFF), 16, G::ATOM_BYTES, G::SWZ);
         const uint64_t dSk = make_sdesc(smem_u32(smem + L::DS_OFF), 16, 1024, SWZ_128B);      // dS^T, K-major
         const uint64_t dSm = make_sdesc(smem_u32(smem + L::DS_OFF), 16384, 1024, SWZ_128B);   // dS, MN-major
-        bool ok = mbar_wait(&bar_kv, 0, &abort_sh, gerr);
-        // dV, dK, dQ of query tile j (stage j % BWD_STAGES)
-        auto finish = [&](int j) -> bool {
-          const int sj = j % BWD_STAGES;
-          const uint64_t qd = desc_add(dQ0, sj * G::TILE_BYTES), od = desc_add(dO0, sj * G::TILE_BYTES);
-          if (!mbar_wait(&bar_pds_full, j & 1, &abort_sh, gerr)) return false;
+        // the step whose dV/dK/dQ are still to be issued
+        struct Pend { int g, st, kb, ic; bool first, last; };
+        bool ok = true;
+        // dV, dK, dQ of step f
+        auto finish = [&](const Pend& f) -> bool {
+          const uint64_t qd = desc_add(dQ0, f.st * G::TILE_BYTES), od = desc_add(dO0, f.st * G::TILE_BYTES);
+          if (!mbar_wait(&bar_pds_full, f.g & 1, &abort_sh, gerr)) return false;
+          // dK/dV of the previous item must have been read out by its epilogue
+          if (f.first && f.ic > 0 && !mbar_wait(&bar_epi_free, (f.ic - 1) & 1, &abort_sh, gerr)) return false;
           tc_fence_after();
           // dV += P^T dO  (A = P^T in TMEM, B = dO MN-major; K = 128 queries)
 #pragma unroll
           for (int k = 0; k < BM / 16; ++k)
             mma_ts(tmem + TB_DV, tmem + TB_P + k * 8, desc_add(od, k * 16 * G::ROW_BYTES), id_kv,
-                   (j > 0 || k > 0) ? 1u : 0u);
+                   (!f.first || k > 0) ? 1u : 0u);
           // dK += dS^T Q  (A = dS^T K-major: 2 blocks of 64 queries, B = Q MN-major)
 #pragma unroll
           for (int k = 0; k < BM / 16; ++k)
             mma_ss(tmem + TB_DK, desc_add(dSk, (k / 4) * 16384 + (k % 4) * 32),
-                   desc_add(qd, k * 16 * G::ROW_BYTES), id_kv, (j > 0 || k > 0) ? 1u : 0u);
-          if (j > 0) {
-            if (!mbar_wait(&bar_dq_free, (j - 1) & 1, &abort_sh, gerr)) return false;
+                   desc_add(qd, k * 16 * G::ROW_BYTES), id_kv, (!f.first || k > 0) ? 1u : 0u);
+          if (f.g > 0) {
+            if (!mbar_wait(&bar_dq_free, (f.g - 1) & 1, &abort_sh, gerr)) return false;
             tc_fence_after();
           }
           // dQ = dS K  (A = dS: MN-major view of the dS^T tile, B = K MN-major; K-dim = 128 keys)
+          const uint64_t kd = desc_add(dK0, f.kb * G::TILE_BYTES);
 #pragma unroll
           for (int k = 0; k < BN / 16; ++k)
-            mma_ss(tmem + TB_DQ, desc_add(dSm, k * 16 * 128), desc_add(dK0, k * 16 * G::ROW_BYTES), id_dq, k > 0);
+            mma_ss(tmem + TB_DQ, desc_add(dSm, k * 16 * 128), desc_add(kd, k * 16 * G::ROW_BYTES), id_dq, k > 0);
           mma_commit(&bar_dq_full);
           // only commits that someone waits for (no arrival after the CTA retires)
-          if (j + 1 < n_it) mma_commit(&bar_pds_free);
-          if (j + BWD_STAGES < n_it) mma_commit(&bar_q_empty[sj]);
+          if (f.g + 1 < total_g) mma_commit(&bar_pds_free);
+          if (f.g + BWD_STAGES < total_g) mma_commit(&bar_q_empty[f.st]);
+          if (f.last) {
+            mma_commit(&bar_done);                           // dK/dV of item f.ic final
+            if (f.ic + 2 < n_items_cta) mma_commit(&bar_kv_empty[f.kb]);
+          }
           return true;
         };
-        for (int it = 0; ok && it < n_it; ++it) {
-          const int st = it % BWD_STAGES;
-          if (!(ok = mbar_wait(&bar_q_full[st], (it / BWD_STAGES) & 1, &abort_sh, gerr))) break;
-          if (it > 0 && !(ok = mbar_wait(&bar_sdp_free, (it - 1) & 1, &abort_sh, gerr))) break;
-          tc_fence_after();
-          const uint64_t qd = desc_add(dQ0, st * G::TILE_BYTES), od = desc_add(dO0, st * G::TILE_BYTES);
-          // S^T = K Q^T ; dP^T = V dO^T   (K-dim = HS)
+        Pend pend{0, 0, 0, 0, false, false};
+        bool have_pend = false;
+        int g = 0;
+        for (int ic = 0; ok && ic < n_items_cta; ++ic) {
+          const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
+          const int kb = ic & 1;
+          if (!(ok = mbar_wait(&bar_kv_full[kb], (ic >> 1) & 1, &abort_sh, gerr))) break;
+          const uint64_t kd = desc_add(dK0, kb * G::TILE_BYTES), vd = desc_add(dV0, kb * G::TILE_BYTES);
+          for (int it = 0; ok && it < w.n_it; ++it, ++g) {
+            const int st = g % BWD_STAGES;
+            if (!(ok = mbar_wait(&bar_q_full[st], (g / BWD_STAGES) & 1, &abort_sh, gerr))) break;
+            if (g > 0 && !(ok = mbar_wait(&bar_sdp_free, (g - 1) & 1, &abort_sh, gerr))) break;
+            tc_fence_after();
+            const uint64_t qd = desc_add(dQ0, st * G::TILE_BYTES), od = desc_add(dO0, st * G::TILE_BYTES);
+            // S^T = K Q^T ; dP^T = V dO^T   (K-dim = HS)
 #pragma unroll
-          for (int k = 0; k < HS / 16; ++k)
-            mma_ss(tmem + TB_S, desc_add(dK0, k * 32), desc_add(qd, k * 32), id_sq, k > 0);
+            for (int k = 0; k < HS / 16; ++k)
+              mma_ss(tmem + TB_S, desc_add(kd, k * 32), desc_add(qd, k * 32), id_sq, k > 0);
 #pragma unroll
-          for (int k = 0; k < HS / 16; ++k)
-            mma_ss(tmem + TB_DP, desc_add(dV0, k * 32), desc_add(od, k * 32), id_sq, k > 0);
-          mma_commit(&bar_sdp_full);
-          if (it > 0) ok = finish(it - 1);
+            for (int k = 0; k < HS / 16; ++k)
+              mma_ss(tmem + TB_DP, desc_add(vd, k * 32), desc_add(od, k * 32), id_sq, k > 0);
+            mma_commit(&bar_sdp_full);
+            if (have_pend) ok = finish(pend);
+            pend = Pend{g, st, kb, ic, it == 0, it == w.n_it - 1};
+            have_pend = true;
+          }
         }
-        if (ok) ok = finish(n_it - 1);
-        if (ok) mma_commit(&bar_done);
+        if (ok && have_pend) ok = finish(pend);
       }
     } else if (warp < 12) {
       // ------------------------------------------------------------ dQ warpgroup
@@ -336,57 +407,58 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
       const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
       const bool leader = (wq == 0 && lane == 0);
       uint8_t* sdq = smem + L::DQ_OFF;
+      const float s = p.scale;
+      int g = 0;
       bool ok = true;
-      for (int it = 0; it < n_it; ++it) {
-        const int qi = i0 + it;
-        ok = mbar_wait(&bar_dq_full, it & 1, &abort_sh, gerr);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t a[HS / 32][32];
+      for (int ic = 0; ok && ic < n_items_cta; ++ic) {
+        const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
+        for (int it = 0; it < w.n_it; ++it, ++g) {
+          const int qi = w.i0 + it;
+          // failures are combined over the warpgroup at the first barrier, so a
+          // bounded wait that gave up never leaves a thread stuck at a barrier
+          const bool fail = !mbar_wait(&bar_dq_full, g & 1, &abort_sh, gerr);
+          tc_fence_after();
+          uint32_t a[HS / 32][32];
 #pragma unroll
-        for (int cc = 0; cc < HS / 32; ++cc) tmem_ld32(tmem + lane_off + TB_DQ + cc * 32, a[cc]);
-        tmem_ld_wait(a[0]);
-        if constexpr (HS == 64) tmem_tie32(a[HS / 32 - 1]);
-        tc_fence_before();
-        mbar_arrive(&bar_dq_free);
-        // the previous bulk reduction must have finished reading the staging tile
-        if (leader) bulk_wait_group_read0();
-        named_bar_sync(1, 128);
-        const float s = p.scale;
+          for (int cc = 0; cc < HS / 32; ++cc) tmem_ld32(tmem + lane_off + TB_DQ + cc * 32, a[cc]);
+          tmem_ld_wait(a[0]);
+          if constexpr (HS == 64) tmem_tie32(a[HS / 32 - 1]);
+          tc_fence_before();
+          mbar_arrive(&bar_dq_free);
+          // the previous bulk operation must have finished reading the staging tile
+          if (leader) bulk_wait_group_read0();
+          if (named_bar_red_or(1, 128, fail)) { ok = false; break; }
 #pragma unroll
-        for (int cc = 0; cc < HS / 32; ++cc) {
-          uint8_t* blk = sdq + cc * 16384;           // [128 q][32 fp32], 128-byte swizzle
+          for (int cc = 0; cc < HS / 32; ++cc) {
+            uint8_t* blk = sdq + cc * 16384;           // [128 q][32 fp32], 128-byte swizzle
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const float4 v = make_float4(__uint_as_float(a[cc][ch * 4 + 0]) * s, __uint_as_float(a[cc][ch * 4 + 1]) * s,
-                                         __uint_as_float(a[cc][ch * 4 + 2]) * s, __uint_as_float(a[cc][ch * 4 + 3]) * s);
-            *reinterpret_cast<float4*>(blk + swz_chunk_offset<64>(r, ch)) = v;
+            for (int ch = 0; ch < 8; ++ch) {
+              const float4 v = make_float4(__uint_as_float(a[cc][ch * 4 + 0]) * s, __uint_as_float(a[cc][ch * 4 + 1]) * s,
+                                           __uint_as_float(a[cc][ch * 4 + 2]) * s, __uint_as_float(a[cc][ch * 4 + 3]) * s);
+              *reinterpret_cast<float4*>(blk + swz_chunk_offset<64>(r, ch)) = v;
+            }
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (leader) {
+#pragma unroll
+            for (int cc = 0; cc < HS / 32; ++cc)
+              tma_reduce_add_3d(&map_dqacc, sdq + cc * 16384, w.h * HS + cc * 32, qi * BM, w.b);
+            bulk_commit_group();
           }
         }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (leader) {
-#pragma unroll
-          for (int cc = 0; cc < HS / 32; ++cc)
-            tma_reduce_add_3d(&map_dqacc, sdq + cc * 16384, h * HS + cc * 32, qi * BM, b);
-          bulk_commit_group();
-        }
-      }
-      if (leader) bulk_wait_group0();
-      // ---------------------------------------------------------- dK, dV epilogue
-      if (ok) {
-        ok = mbar_wait(&bar_done, 0, &abort_sh, gerr);
-        ok = __all_sync(0xffffffffu, ok);
-      }
-      if (ok) {
+        if (!ok) break;
+        // ---------------------------------------------------------- dK, dV of this item
+        const bool fail = !mbar_wait(&bar_done, ic & 1, &abort_sh, gerr);
         tc_fence_after();
-        uint8_t* stage_v = smem + L::DS_OFF;         // dS^T tile is dead after the last MMA
-        uint8_t* stage_k = smem + L::DS_OFF + 16384;
+        if (leader) bulk_wait_group_read0();             // staging free for dK/dV
+        if (named_bar_red_or(1, 128, fail)) { ok = false; break; }
+        uint8_t* stage_v = sdq;
+        uint8_t* stage_k = sdq + G::TILE_BYTES;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           const uint32_t col = which == 0 ? TB_DV : TB_DK;
-          const float mul = which == 0 ? 1.f : p.scale;
+          const float mul = which == 0 ? 1.f : s;
           uint8_t* stage = which == 0 ? stage_v : stage_k;
 #pragma unroll
           for (int cc = 0; cc < HS; cc += 32) {
@@ -404,69 +476,76 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
             }
           }
         }
+        tc_fence_before();
+        // every commit is awaited: only signal if the MMA warp will wait for it
+        if (ic + 1 < n_items_cta) mbar_arrive(&bar_epi_free);   // dK/dV TMEM columns free
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (leader) {
-          tma_store_3d(&map_dqkv, stage_v, 2 * p.C + h * HS, kv * BN, b);
-          tma_store_3d(&map_dqkv, stage_k, p.C + h * HS, kv * BN, b);
+          tma_store_3d(&map_dqkv, stage_v, 2 * p.C + w.h * HS, w.kv * BN, w.b);
+          tma_store_3d(&map_dqkv, stage_k, p.C + w.h * HS, w.kv * BN, w.b);
           bulk_commit_group();
-          bulk_wait_group_read0();
         }
       }
+      if (leader) bulk_wait_group0();
     }
   } else {
     setmaxnreg_inc<REG_SOFTMAX>();
     // ------------------------------------------------------------ softmax warpgroups
     const int half = warp >> 2;                    // query columns [64*half, 64*half+64)
     const int r = ((warp & 3) << 5) + lane;        // key row in the tile = TMEM lane
-    const int key = kv * BN + r;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float c = p.scale_log2;
     uint8_t* sds = smem + L::DS_OFF + half * 16384;
-    for (int it = 0; it < n_it; ++it) {
-      const int st = it % BWD_STAGES;
-      const int qi = i0 + it;
-      bool ok = mbar_wait(&bar_q_full[st], (it / BWD_STAGES) & 1, &abort_sh, gerr);
-      ok = ok && mbar_wait(&bar_sdp_full, it & 1, &abort_sh, gerr);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sv[2][32], dpv[2][32];
-      tmem_ld32(tmem + lane_off + TB_S + half * 64, sv[0]);
-      tmem_ld32(tmem + lane_off + TB_S + half * 64 + 32, sv[1]);
-      tmem_ld32(tmem + lane_off + TB_DP + half * 64, dpv[0]);
-      tmem_ld32(tmem + lane_off + TB_DP + half * 64 + 32, dpv[1]);
-      tmem_ld_wait(sv[0]);
-      tmem_tie32(sv[1]);
-      tmem_tie32(dpv[0]);
-      tmem_tie32(dpv[1]);
-      tc_fence_before();
-      mbar_arrive(&bar_sdp_free);                  // S^T/dP^T columns may be overwritten now
-      const float* rs = reinterpret_cast<const float*>(smem + L::ROWST_OFF) + st * 256 + half * 64;
-      const bool diag = CAUSAL && (qi == kv);
-      uint32_t pk[32], dk[32];
-      // masked variant only on the diagonal tile or a tile with keys past T
-      if (__any_sync(0xffffffffu, diag || key >= T))
-        bwd_p_ds<true>(sv, dpv, rs, c, half * 64, r, diag, key < T, pk, dk);
-      else
-        bwd_p_ds<false>(sv, dpv, rs, c, half * 64, r, false, true, pk, dk);
-      if (it > 0) {
-        ok = mbar_wait(&bar_pds_free, (it - 1) & 1, &abort_sh, gerr);
+    int g = 0;
+    bool ok = true;
+    for (int ic = 0; ok && ic < n_items_cta; ++ic) {
+      const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
+      const int key = w.kv * BN + r;
+      for (int it = 0; it < w.n_it; ++it, ++g) {
+        const int st = g % BWD_STAGES;
+        const int qi = w.i0 + it;
+        ok = mbar_wait(&bar_q_full[st], (g / BWD_STAGES) & 1, &abort_sh, gerr);
+        ok = ok && mbar_wait(&bar_sdp_full, g & 1, &abort_sh, gerr);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-      }
-      tmem_st32(tmem + lane_off + TB_P + half * 32, pk);
-      // dS^T row `r`, queries [64*half, 64*half+64): block `half`, 8 chunks of 16 bytes
+        uint32_t sv[2][32], dpv[2][32];
+        tmem_ld32(tmem + lane_off + TB_S + half * 64, sv[0]);
+        tmem_ld32(tmem + lane_off + TB_S + half * 64 + 32, sv[1]);
+        tmem_ld32(tmem + lane_off + TB_DP + half * 64, dpv[0]);
+        tmem_ld32(tmem + lane_off + TB_DP + half * 64 + 32, dpv[1]);
+        tmem_ld_wait(sv[0]);
+        tmem_tie32(sv[1]);
+        tmem_tie32(dpv[0]);
+        tmem_tie32(dpv[1]);
+        tc_fence_before();
+        mbar_arrive(&bar_sdp_free);                  // S^T/dP^T columns may be overwritten now
+        const float* rs = reinterpret_cast<const float*>(smem + L::ROWST_OFF) + st * 256 + half * 64;
+        const bool diag = CAUSAL && (qi == w.kv);
+        uint32_t pk[32], dk[32];
+        // masked variant only on the diagonal tile or a tile with keys past T
+        if (__any_sync(0xffffffffu, diag || key >= T))
+          bwd_p_ds<true>(sv, dpv, rs, c, half * 64, r, diag, key < T, pk, dk);
+        else
+          bwd_p_ds<false>(sv, dpv, rs, c, half * 64, r, false, true, pk, dk);
+        if (g > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_pds_free, (g - 1) & 1, &abort_sh, gerr));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        tmem_st32(tmem + lane_off + TB_P + half * 32, pk);
+        // dS^T row `r`, queries [64*half, 64*half+64): block `half`, 8 chunks of 16 bytes
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint4 v = make_uint4(dk[ch * 4 + 0], dk[ch * 4 + 1], dk[ch * 4 + 2], dk[ch * 4 + 3]);
-        *reinterpret_cast<uint4*>(sds + swz_chunk_offset<64>(r, ch)) = v;
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 v = make_uint4(dk[ch * 4 + 0], dk[ch * 4 + 1], dk[ch * 4 + 2], dk[ch * 4 + 3]);
+          *reinterpret_cast<uint4*>(sds + swz_chunk_offset<64>(r, ch)) = v;
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bar_pds_full);
       }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bar_pds_full);
     }
   }
 
@@ -524,9 +603,11 @@ cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_d
   p.C = pr.C;
   p.n_kv = (pr.T + BN - 1) / BN;
   p.BH = pr.B * pr.NH;
+  p.n_items = p.n_kv * p.BH;
   p.scale = (float)(1.0 / __builtin_sqrt((double)pr.hs));
   p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)pr.hs));
-  const int grid = p.n_kv * p.BH;
+  const int n_sm = device_sm_count();
+  const int grid = p.n_items < n_sm ? p.n_items : n_sm;   // persistent: one CTA per SM
   if (pr.hs == 64)
     e = pr.causal ? launch_bwd_main<64, true>(map_qkv, map_dout, map_dqkv, map_dqacc, p, grid, stream)
                   : launch_bwd_main<64, false>(map_qkv, map_dout, map_dqkv, map_dqacc, p, grid, stream);

@@ -41,6 +41,9 @@ struct Problem {
 // attn_status_t code written by a kernel whose bounded wait gave up).
 int* device_error_word();
 
+// Number of SMs of the current device (cached; persistent grids are sized by it).
+int device_sm_count();
+
 // Optional per-kernel timing (see attn_profile_enable in include/attn.h).
 enum KernelId { K_FWD = 0, K_BWD_PRE = 1, K_BWD_MAIN = 2, K_BWD_DQ = 3, K_COUNT = 4 };
 void profile_begin(KernelId k, cudaStream_t s);
