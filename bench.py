@@ -3,9 +3,14 @@
 One step = attn_fwd + attn_bwd (every kernel of the hot path) over one batch
 of the GPT-2 small attention layer, bf16: B=16, T=1024, C=768, NH=12 (hs=64),
 causal. Metric: causal-adjusted TFLOP/s, FLOPs counted the FlashAttention way:
-fwd = 4*B*NH*T^2*hs/2, bwd = 2.5*fwd, step = 3.5*fwd.
+fwd = 4*B*NH*T^2*hs/2 (x2 without the mask), bwd = 2.5*fwd, step = 3.5*fwd.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload NAME]
+
+--workload times another of the attention-layer shapes (inputs.WORKLOADS,
+e.g. gpt2s_f32 for fp32 inputs on the tf32 tensor-core path); the default is
+the GPT-2 small bf16 layer the metric is quoted on.
 
 Prints ONE JSON line (rank 0). For N>1 launch with torch.distributed.run; each
 rank runs its own independent batch (weak scaling, no collective on the data
@@ -29,6 +34,7 @@ sys.path.insert(0, str(ROOT))
 WORKLOAD = "gpt2s_bf16"
 METRIC = "attention fwd+bwd causal TFLOP/s at 1 GB300 and % of dense tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TF32_PER_BF16 = 1.1 / 2.25    # nominal dense tf32 / bf16 tensor rate of the GB300
 FLUSH_BYTES = 512 << 20   # > 129 MB L2
 
 
@@ -180,8 +186,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     from causal_head_attention_fwd_gb300 import inputs
-    w = inputs.WORKLOADS[WORKLOAD]
-    res, cores = run_oracle_child(WORKLOAD, 1e9, args.warmup + args.steps)
+    w = inputs.WORKLOADS[args.workload]
+    res, cores = run_oracle_child(args.workload, 1e9, args.warmup + args.steps)
     times = res["step_times"][args.warmup:]
     f_head = flops(1, w.T, w.C, w.NH, w.causal)["step"] / w.NH
     t = sum(times) / len(times)
@@ -192,7 +198,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(w),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"one (b,h) head of {WORKLOAD} per step (1/{w.B * w.NH} of the batch), "
+                         "sample": f"one (b,h) head of {w.name} per step (1/{w.B * w.NH} of the batch), "
                                    "fwd+bwd, float64 numpy oracle"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -201,8 +207,9 @@ def run_reference(args):
 
 
 def config_dict(w):
-    return {"workload": f"{w.name}: GPT-2 small attention layer, B={w.B} T={w.T} C={w.C} NH={w.NH} "
-                        f"hs={w.hs}, causal, bf16 qkv~N(0,{w.sigma_qkv}^2) dout~N(0,{w.sigma_dout}^2)",
+    mask = "causal" if w.causal else "non-causal"
+    return {"workload": f"{w.name}: attention layer, B={w.B} T={w.T} C={w.C} NH={w.NH} "
+                        f"hs={w.hs}, {mask}, {w.dtype} qkv~N(0,{w.sigma_qkv}^2) dout~N(0,{w.sigma_dout}^2)",
             "B": w.B, "T": w.T, "C": w.C, "NH": w.NH, "causal": w.causal,
             "l2": "flushed between timed steps (512 MiB write)"}
 
@@ -215,6 +222,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -234,23 +242,27 @@ def main(argv=None):
     build.build()
     from causal_head_attention_fwd_gb300 import api, ops
 
-    w = inputs.WORKLOADS[WORKLOAD]
-    B, T, C, NH = w.B, w.T, w.C, w.NH
+    w = inputs.WORKLOADS[args.workload]
+    B, T, C, NH, causal = w.B, w.T, w.C, w.NH, w.causal
+    is_bf16 = w.dtype == "bf16"
+    adt = api.ATTN_BF16 if is_bf16 else api.ATTN_F32
+    tdt = torch.bfloat16 if is_bf16 else torch.float32
+    esz = 2 if is_bf16 else 4
     host = inputs.make_inputs(B, T, C, NH, w.dtype, w.sigma_qkv, w.sigma_dout,
                               w.seed_qkv + 7919 * rank, w.seed_dout + 7919 * rank)
-    qkv = ops.upload(host.qkv_dev, "bf16", dev)
-    dout = ops.upload(host.dout_dev, "bf16", dev)
-    out = torch.empty((B, T, C), dtype=torch.bfloat16, device=dev)
+    qkv = ops.upload(host.qkv_dev, w.dtype, dev)
+    dout = ops.upload(host.dout_dev, w.dtype, dev)
+    out = torch.empty((B, T, C), dtype=tdt, device=dev)
     lse = torch.empty((B, NH, T), dtype=torch.float32, device=dev)
     dqkv = torch.empty_like(qkv)
-    ws_bytes = api.attn_bwd_workspace_size(B, T, C, NH, 1, api.ATTN_BF16)
+    ws_bytes = api.attn_bwd_workspace_size(B, T, C, NH, causal, adt)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        api.attn_fwd(qkv, out, lse, B, T, C, NH, 1, api.ATTN_BF16, stream)
-        api.attn_bwd(dout, qkv, out, lse, dqkv, B, T, C, NH, 1, api.ATTN_BF16, ws, ws_bytes, stream)
+        api.attn_fwd(qkv, out, lse, B, T, C, NH, causal, adt, stream)
+        api.attn_bwd(dout, qkv, out, lse, dqkv, B, T, C, NH, causal, adt, ws, ws_bytes, stream)
 
     def barrier():
         if world > 1:
@@ -282,7 +294,7 @@ def main(argv=None):
     if api.attn_last_device_error(stream) != api.ATTN_OK:
         raise RuntimeError("device error in the timed region")
     t_ms = sum(times) / len(times)
-    f = flops(B, T, C, NH, 1)
+    f = flops(B, T, C, NH, causal)
     value_flops, t_max = aggregate(f["step"], t_ms, world, dev)
     value = value_flops / 1e12
 
@@ -292,7 +304,7 @@ def main(argv=None):
     timed(max(20, min(args.steps, 200)), step)
     api.attn_profile_enable(False)
     kern = {}
-    for kid, name in api.KERNEL_NAMES.items():
+    for kid, name in (api.KERNEL_NAMES if is_bf16 else api.KERNEL_NAMES_F32).items():
         ms, n = api.attn_profile_read(kid)
         kern[name] = {"launches": n, "avg_ms": ms / max(n, 1)}
     tot = sum(k["avg_ms"] for k in kern.values())
@@ -300,37 +312,43 @@ def main(argv=None):
         k["share"] = k["avg_ms"] / tot if tot > 0 else None
     peaks, peak_src = load_peaks()
     dom = max(kern, key=lambda k: kern[k]["avg_ms"])
-    dom_flops = {"attn_fwd_kernel": f["fwd"], "attn_bwd_kernel": f["bwd"]}.get(dom)
-    peak_tf = float(peaks["bf16_tflops"])
+    # algorithmic FLOPs per launch; the fp32 backward splits the five matmuls
+    # into dK/dV (S, dP, dV, dK) and dQ (dQ; its S and dP recompute is not counted)
+    dom_flops = {"attn_fwd_kernel": f["fwd"], "attn_bwd_kernel": f["bwd"], "attn_fwd_f32_kernel": f["fwd"],
+                 "attn_bwd_dkdv_f32": 2.0 * f["fwd"], "attn_bwd_dq_f32": 0.5 * f["fwd"]}.get(dom)
+    peak_tf = float(peaks["bf16_tflops"]) * (1.0 if is_bf16 else TF32_PER_BF16)
     if dom_flops is not None:
         ach = dom_flops / (kern[dom]["avg_ms"] * 1e-3) / 1e12
+        src = (f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)" if peak_src == "measured"
+               else "fallback 1.9 PFLOP/s bf16")
+        if not is_bf16:
+            src = f"tf32 = {src} x nominal 1.1/2.25"
         roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak_tf, "unit": "TFLOP/s",
-                    "frac": ach / peak_tf, "traffic": None,
-                    "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
-                    if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16"}
+                    "frac": ach / peak_tf, "traffic": None, "peak_source": src}
     else:
         roofline = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": float(peaks["hbm_gbs"]),
                     "unit": "GB/s", "frac": None, "traffic": None}
     traffic_file = ROOT / "profiles" / "traffic.json"
     if traffic_file.exists():
         tr = json.loads(traffic_file.read_text()).get(dom)
-        if tr and tr.get("source_hash") == kernel_source_hash():
+        if tr and tr.get("source_hash") == kernel_source_hash(dom):
             roofline["traffic"] = tr["bytes_per_launch"]
-    fwd_ms = kern["attn_fwd_kernel"]["avg_ms"]
-    bwd_ms = sum(kern[k]["avg_ms"] for k in ("attn_bwd_pre", "attn_bwd_kernel", "attn_bwd_dq_out"))
-    ab = algo_bytes(B, T, C, NH, 2)
+    names = list(kern)
+    fwd_ms = kern[names[0]]["avg_ms"]
+    bwd_ms = sum(kern[k]["avg_ms"] for k in names[1:])
+    ab = algo_bytes(B, T, C, NH, esz)
 
     # ---- end to end through the public API with host buffers
-    h_qkv = ops.upload(host.qkv_dev, "bf16", pin=True)
-    h_dout = ops.upload(host.dout_dev, "bf16", pin=True)
-    h_out = torch.empty((B, T, C), dtype=torch.bfloat16).pin_memory()
-    h_dqkv = torch.empty((B, T, 3 * C), dtype=torch.bfloat16).pin_memory()
+    h_qkv = ops.upload(host.qkv_dev, w.dtype, pin=True)
+    h_dout = ops.upload(host.dout_dev, w.dtype, pin=True)
+    h_out = torch.empty((B, T, C), dtype=tdt).pin_memory()
+    h_dqkv = torch.empty((B, T, 3 * C), dtype=tdt).pin_memory()
 
     def e2e_step():
         qkv.copy_(h_qkv, non_blocking=True)
         dout.copy_(h_dout, non_blocking=True)
-        ops.attention_forward(qkv, NH, True, out=out, lse=lse, stream=stream)
-        ops.attention_backward(dout, qkv, out, lse, NH, True, dqkv=dqkv, stream=stream)
+        ops.attention_forward(qkv, NH, bool(causal), out=out, lse=lse, stream=stream)
+        ops.attention_backward(dout, qkv, out, lse, NH, bool(causal), dqkv=dqkv, stream=stream)
         h_out.copy_(out, non_blocking=True)
         h_dqkv.copy_(dqkv, non_blocking=True)
 
@@ -343,20 +361,20 @@ def main(argv=None):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(w),
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": config_dict(w),
         "pct_of_peak": value / peak_tf,
         "fwd_tflops": f["fwd"] / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": f["bwd"] / (bwd_ms * 1e-3) / 1e12,
         "fwd_hbm_gbs": ab["fwd"] / (fwd_ms * 1e-3) / 1e9, "bwd_hbm_gbs": ab["bwd"] / (bwd_ms * 1e-3) / 1e9,
         "roofline": roofline, "kernels": kern,
         "e2e": {"value": e2e_val / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": int(qkv.numel() * 2 + dout.numel() * 2),
-                "d2h_bytes_per_step": int(out.numel() * 2 + dqkv.numel() * 2),
+                "h2d_bytes_per_step": int((qkv.numel() + dout.numel()) * esz),
+                "d2h_bytes_per_step": int((out.numel() + dqkv.numel()) * esz),
                 "ms_per_step": e2e_ms},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(WORKLOAD)
+        line["cpu_baseline"] = cpu_baseline(args.workload)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -365,13 +383,22 @@ def main(argv=None):
     return 0
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources; ties a stored ncu traffic figure to the kernel it measured."""
+# CUDA sources each kernel is compiled from (its translation unit and headers)
+_KERNEL_SOURCES = {
+    "bf16": ["attn_fwd.cu", "attn_bwd.cu", "common.cuh", "ptx.cuh"],
+    "f32": ["attn_f32.cu", "tf32.cuh", "common.cuh", "ptx.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str = "attn_bwd_kernel") -> str:
+    """Hash of the CUDA sources a kernel is built from; ties a stored ncu
+    traffic figure to the kernel version it measured."""
     import hashlib
     h = hashlib.sha256()
-    for p in sorted((ROOT / "causal_head_attention_fwd_gb300" / "csrc").glob("*")):
-        h.update(p.name.encode())
-        h.update(p.read_bytes())
+    csrc = ROOT / "causal_head_attention_fwd_gb300" / "csrc"
+    for name in _KERNEL_SOURCES["f32" if "f32" in kernel else "bf16"]:
+        h.update(name.encode())
+        h.update((csrc / name).read_bytes())
     return h.hexdigest()[:16]
 
 

@@ -36,6 +36,9 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 K_FWD, K_BWD_PRE, K_BWD_MAIN, K_BWD_DQ = 0, 1, 2, 3
 KERNEL_NAMES = {K_FWD: "attn_fwd_kernel", K_BWD_PRE: "attn_bwd_pre",
                 K_BWD_MAIN: "attn_bwd_kernel", K_BWD_DQ: "attn_bwd_dq_out"}
+# The same four profiling slots hold the fp32 path's kernels.
+KERNEL_NAMES_F32 = {K_FWD: "attn_fwd_f32_kernel", K_BWD_PRE: "attn_bwd_pre_f32",
+                    K_BWD_MAIN: "attn_bwd_dkdv_f32", K_BWD_DQ: "attn_bwd_dq_f32"}
 
 
 class AttnError(RuntimeError):

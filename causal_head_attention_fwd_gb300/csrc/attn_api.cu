@@ -22,6 +22,12 @@ cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_d
                             const CUtensorMap& map_dqkv, const CUtensorMap& map_dqacc, const void* dout,
                             const void* out, const float* lse, void* dqkv, float* ws_D, float* ws_dq,
                             const Problem& pr, cudaStream_t stream);
+cudaError_t launch_fwd_f32(const CUtensorMap& map_q_l, const CUtensorMap& map_q_s, const CUtensorMap& map_out_l,
+                           float* lse, const Problem& pr, cudaStream_t stream);
+cudaError_t launch_bwd_f32(const CUtensorMap& map_q_l, const CUtensorMap& map_q_s, const CUtensorMap& map_do_l,
+                           const CUtensorMap& map_do_s, const CUtensorMap& map_g_l, const float* dout,
+                           const float* out, const float* lse, float* ws_D, const Problem& pr,
+                           cudaStream_t stream);
 
 static __device__ int g_error_word = 0;
 
@@ -146,11 +152,12 @@ static attn_status_t check_shape(int B, int T, int C, int NH, int causal, attn_d
   if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
   const int hs = C / NH;
   if (hs != 32 && hs != 64) return ATTN_ERR_UNSUPPORTED;
-  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   // element counts must fit the 32-bit grid/tile arithmetic of the kernels
   const double n3 = (double)B * T * 3.0 * C;
   if (n3 > 9.0e15 || (double)T > 2.0e9 || (double)B * NH * ((T + 255) / 256) > 2.0e9)
     return ATTN_ERR_INVALID_ARG;
+  // the fp32 backward launches one CTA per (b, h, 128-row tile)
+  if (dtype == ATTN_F32 && (double)B * NH * ((T + 127) / 128) > 2.0e9) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
@@ -191,6 +198,17 @@ extern "C" attn_status_t attn_fwd(const void* qkv, void* out, float* lse, int B,
     return ATTN_ERR_INVALID_ARG;
   Problem pr{B, T, C, NH, C / NH, causal};
   if (!device_error_word() || device_sm_count() <= 0) return ATTN_ERR_CUDA;
+  if (dtype == ATTN_F32) {
+    // fp32 tiles: 32-column (128-byte) boxes, 128- or 64-row
+    const CUtensorMapDataType f = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUtensorMapSwizzle w = CU_TENSOR_MAP_SWIZZLE_128B;
+    CUtensorMap ql, qs, ol;
+    if (!encode_3d(&ql, qkv, f, 4, 3 * C, T, B, 32, 128, w) || !encode_3d(&qs, qkv, f, 4, 3 * C, T, B, 32, 64, w) ||
+        !encode_3d(&ol, out, f, 4, C, T, B, 32, 128, w))
+      return ATTN_ERR_CUDA;
+    cudaError_t ce = launch_fwd_f32(ql, qs, ol, lse, pr, static_cast<cudaStream_t>(stream));
+    return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
   const CUtensorMapSwizzle swz = pr.hs == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap mq, mo;
   if (!encode_3d(&mq, qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3 * C, T, B, pr.hs, BM, swz) ||
@@ -202,8 +220,10 @@ extern "C" attn_status_t attn_fwd(const void* qkv, void* out, float* lse, int B,
 
 extern "C" size_t attn_bwd_workspace_size(int B, int T, int C, int NH, int causal, attn_dtype_t dtype) {
   if (check_shape(B, T, C, NH, causal, dtype) != ATTN_OK) return 0;
-  // D (B*NH*T fp32) rounded to 256 bytes, then the fp32 dq accumulator (B*T*C)
+  // D (B*NH*T fp32) rounded to 256 bytes; bf16 adds the fp32 dq accumulator
+  // (B*T*C); the fp32 path writes dq straight into dqkv
   const size_t d_bytes = (((size_t)B * NH * T * 4) + 255) & ~(size_t)255;
+  if (dtype == ATTN_F32) return d_bytes;
   return d_bytes + (size_t)B * T * C * 4;
 }
 
@@ -225,6 +245,19 @@ extern "C" attn_status_t attn_bwd(const void* dout, const void* qkv, const void*
     return ATTN_ERR_INVALID_ARG;
   Problem pr{B, T, C, NH, C / NH, causal};
   if (!device_error_word() || device_sm_count() <= 0) return ATTN_ERR_CUDA;
+  if (dtype == ATTN_F32) {
+    const CUtensorMapDataType f = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUtensorMapSwizzle w = CU_TENSOR_MAP_SWIZZLE_128B;
+    CUtensorMap ql, qs, dl, ds, gl;
+    if (!encode_3d(&ql, qkv, f, 4, 3 * C, T, B, 32, 128, w) || !encode_3d(&qs, qkv, f, 4, 3 * C, T, B, 32, 64, w) ||
+        !encode_3d(&dl, dout, f, 4, C, T, B, 32, 128, w) || !encode_3d(&ds, dout, f, 4, C, T, B, 32, 64, w) ||
+        !encode_3d(&gl, dqkv, f, 4, 3 * C, T, B, 32, 128, w))
+      return ATTN_ERR_CUDA;
+    cudaError_t ce = launch_bwd_f32(ql, qs, dl, ds, gl, static_cast<const float*>(dout),
+                                    static_cast<const float*>(out), lse, static_cast<float*>(workspace), pr,
+                                    static_cast<cudaStream_t>(stream));
+    return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
   const CUtensorMapSwizzle swz = pr.hs == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap mq, md, mg;
   if (!encode_3d(&mq, qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3 * C, T, B, pr.hs, BM, swz) ||
