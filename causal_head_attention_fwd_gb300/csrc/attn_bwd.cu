@@ -28,7 +28,7 @@
 //   warps 4-7   softmax warpgroup B: query columns [64, 128)
 //   warps 8-11  dQ warpgroup: thread = query row; TMEM -> smem -> TMA reduce-add;
 //               after each item the dK/dV epilogue (thread = key row)
-//   warp  12    loader: K, V per item; Q, dO, lse, D per query tile (2-stage ring)
+//   warp  12    loader: K, V per item; Q, dO, lse, D per query tile (3-stage ring)
 //   warp  13    MMA issuer; warps 14-15 idle
 // The softmax warpgroups copy S^T/dP^T of step g into registers and release
 // them at once, so the tensor core computes S^T/dP^T of step g+1 while P/dS of
@@ -39,7 +39,7 @@
 
 namespace attn {
 
-constexpr int BWD_STAGES = 2;
+constexpr int BWD_STAGES = 3;
 constexpr int BWD_THREADS = 512;
 constexpr uint32_t TB_S = 0, TB_DP = 128, TB_P = 256, TB_DV = 320, TB_DK = 384, TB_DQ = 448;
 // register split: 2 softmax warpgroups up, the other 2 warpgroups down.
@@ -56,12 +56,13 @@ struct BwdSmem {
   static constexpr int DO_OFF = Q_OFF + BWD_STAGES * TILE;     // BWD_STAGES tiles
   static constexpr int DS_OFF = DO_OFF + BWD_STAGES * TILE;    // dS^T: 2 blocks of [128 keys][64 q] bf16
   static constexpr int DS_BYTES = 2 * 128 * 128;
-  static constexpr int DQ_OFF = DS_OFF + DS_BYTES;             // dQ fp32 [128 q][32] SW128 blocks; dK/dV staging
-  static constexpr int DQ_BYTES = (HS / 32) * 128 * 128;
+  static constexpr int DQ_OFF = DS_OFF + DS_BYTES;             // dQ fp32 [128 q][32] SW128 block; dK/dV staging
+  static constexpr int DQ_BYTES = 128 * 128;
   static constexpr int ROWST_OFF = DQ_OFF + DQ_BYTES;          // per stage: -lse*log2e [128], D [128]
   static constexpr int BYTES = ROWST_OFF + BWD_STAGES * 2 * 128 * 4;
   static constexpr int ALLOC = BYTES + 1024;
-  static_assert(2 * TILE <= DQ_BYTES, "dK/dV staging must fit in the dQ staging area");
+  static_assert(TILE <= DQ_BYTES, "dK/dV staging must fit in the dQ staging area");
+  static_assert(ALLOC <= 227 * 1024, "shared memory budget");
 };
 
 struct BwdParams {
@@ -425,41 +426,39 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
           if constexpr (HS == 64) tmem_tie32(a[HS / 32 - 1]);
           tc_fence_before();
           mbar_arrive(&bar_dq_free);
-          // the previous bulk operation must have finished reading the staging tile
-          if (leader) bulk_wait_group_read0();
-          if (named_bar_red_or(1, 128, fail)) { ok = false; break; }
+          // one 32-column block at a time through the 16 KB staging tile
 #pragma unroll
           for (int cc = 0; cc < HS / 32; ++cc) {
-            uint8_t* blk = sdq + cc * 16384;           // [128 q][32 fp32], 128-byte swizzle
+            // the previous bulk operation must have finished reading the staging tile
+            if (leader) bulk_wait_group_read0();
+            if (named_bar_red_or(1, 128, fail)) { ok = false; break; }
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
+            for (int ch = 0; ch < 8; ++ch) {           // [128 q][32 fp32], 128-byte swizzle
               const float4 v = make_float4(__uint_as_float(a[cc][ch * 4 + 0]) * s, __uint_as_float(a[cc][ch * 4 + 1]) * s,
                                            __uint_as_float(a[cc][ch * 4 + 2]) * s, __uint_as_float(a[cc][ch * 4 + 3]) * s);
-              *reinterpret_cast<float4*>(blk + swz_chunk_offset<64>(r, ch)) = v;
+              *reinterpret_cast<float4*>(sdq + swz_chunk_offset<64>(r, ch)) = v;
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (leader) {
+              tma_reduce_add_3d(&map_dqacc, sdq, w.h * HS + cc * 32, qi * BM, w.b);
+              bulk_commit_group();
             }
           }
-          fence_proxy_async_smem();
-          named_bar_sync(1, 128);
-          if (leader) {
-#pragma unroll
-            for (int cc = 0; cc < HS / 32; ++cc)
-              tma_reduce_add_3d(&map_dqacc, sdq + cc * 16384, w.h * HS + cc * 32, qi * BM, w.b);
-            bulk_commit_group();
-          }
+          if (!ok) break;
         }
         if (!ok) break;
         // ---------------------------------------------------------- dK, dV of this item
         const bool fail = !mbar_wait(&bar_done, ic & 1, &abort_sh, gerr);
         tc_fence_after();
-        if (leader) bulk_wait_group_read0();             // staging free for dK/dV
-        if (named_bar_red_or(1, 128, fail)) { ok = false; break; }
-        uint8_t* stage_v = sdq;
-        uint8_t* stage_k = sdq + G::TILE_BYTES;
+        // dV, then scale*dK, through the staging tile
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
+          if (leader) bulk_wait_group_read0();           // staging free
+          if (named_bar_red_or(1, 128, fail)) { ok = false; break; }
           const uint32_t col = which == 0 ? TB_DV : TB_DK;
           const float mul = which == 0 ? 1.f : s;
-          uint8_t* stage = which == 0 ? stage_v : stage_k;
+          uint8_t* stage = sdq;
 #pragma unroll
           for (int cc = 0; cc < HS; cc += 32) {
             uint32_t o[32];
@@ -475,17 +474,19 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
               *reinterpret_cast<uint4*>(stage + swz_chunk_offset<HS>(r, cc / 8 + ch)) = v;
             }
           }
+          if (which == 1) {
+            tc_fence_before();
+            // every commit is awaited: only signal if the MMA warp will wait for it
+            if (ic + 1 < n_items_cta) mbar_arrive(&bar_epi_free);   // dK/dV TMEM columns free
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (leader) {
+            tma_store_3d(&map_dqkv, stage, (which == 0 ? 2 * p.C : p.C) + w.h * HS, w.kv * BN, w.b);
+            bulk_commit_group();
+          }
         }
-        tc_fence_before();
-        // every commit is awaited: only signal if the MMA warp will wait for it
-        if (ic + 1 < n_items_cta) mbar_arrive(&bar_epi_free);   // dK/dV TMEM columns free
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (leader) {
-          tma_store_3d(&map_dqkv, stage_v, 2 * p.C + w.h * HS, w.kv * BN, w.b);
-          tma_store_3d(&map_dqkv, stage_k, p.C + w.h * HS, w.kv * BN, w.b);
-          bulk_commit_group();
-        }
+        if (!ok) break;
       }
       if (leader) bulk_wait_group0();
     }
