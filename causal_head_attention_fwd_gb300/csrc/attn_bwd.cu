@@ -236,13 +236,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
       mbar_init(&bar_q_empty[s], 1);
     }
     mbar_init(&bar_sdp_full, 1);
-    mbar_init(&bar_sdp_free, 256);
-    mbar_init(&bar_pds_full, 256);
+    mbar_init(&bar_sdp_free, 8);                 // one arrival per softmax warp
+    mbar_init(&bar_pds_full, 8);
     mbar_init(&bar_pds_free, 1);
     mbar_init(&bar_dq_full, 1);
-    mbar_init(&bar_dq_free, 128);
+    mbar_init(&bar_dq_free, 4);                  // one arrival per dQ warp
     mbar_init(&bar_done, 1);
-    mbar_init(&bar_epi_free, 128);
+    mbar_init(&bar_epi_free, 4);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -425,7 +425,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
           tmem_ld_wait(a[0]);
           if constexpr (HS == 64) tmem_tie32(a[HS / 32 - 1]);
           tc_fence_before();
-          mbar_arrive(&bar_dq_free);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_dq_free);
           // one 32-column block at a time through the 16 KB staging tile
 #pragma unroll
           for (int cc = 0; cc < HS / 32; ++cc) {
@@ -477,7 +478,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
           if (which == 1) {
             tc_fence_before();
             // every commit is awaited: only signal if the MMA warp will wait for it
-            if (ic + 1 < n_items_cta) mbar_arrive(&bar_epi_free);   // dK/dV TMEM columns free
+            __syncwarp();
+            if (lane == 0 && ic + 1 < n_items_cta) mbar_arrive(&bar_epi_free);   // dK/dV TMEM columns free
           }
           fence_proxy_async_smem();
           named_bar_sync(1, 128);
@@ -521,7 +523,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
         tmem_tie32(dpv[0]);
         tmem_tie32(dpv[1]);
         tc_fence_before();
-        mbar_arrive(&bar_sdp_free);                  // S^T/dP^T columns may be overwritten now
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_sdp_free);   // S^T/dP^T columns may be overwritten now
         const float* rs = reinterpret_cast<const float*>(smem + L::ROWST_OFF) + st * 256 + half * 64;
         const bool diag = CAUSAL && (qi == w.kv);
         uint32_t pk[32], dk[32];
@@ -545,7 +548,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&bar_pds_full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_pds_full);
       }
     }
   }

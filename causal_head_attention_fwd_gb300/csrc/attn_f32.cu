@@ -99,7 +99,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[2][32]) 
 }
 
 constexpr int NT = 2;                 // transposer warps per CTA
-constexpr int NT_THREADS = NT * 32;
 
 // One 32x32 sub-block `sb` of the transpose of a streamed [64 rows][HS] tile
 // (HS/32 blocks of [64][32]) into [HS rows][64] (2 blocks of [HS][32]), both
@@ -194,16 +193,16 @@ attn_fwd_f32_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     for (int s = 0; s < ST; ++s) {
       mbar_init(&bar_k_full[s], 1);
       mbar_init(&bar_v_full[s], 1);
-      mbar_init(&bar_kv_empty[s], 1 + NT_THREADS);   // K by the MMAs, V by the transposers
+      mbar_init(&bar_kv_empty[s], 1 + NT);           // K by the MMAs, V by the transposer warps
     }
     for (int s = 0; s < ST2; ++s) {
-      mbar_init(&bar_vt_full[s], NT_THREADS);
+      mbar_init(&bar_vt_full[s], NT);
       mbar_init(&bar_vt_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_s[i][0], 1);
       mbar_init(&bar_s[i][1], 1);
-      mbar_init(&bar_p[i], 128);
+      mbar_init(&bar_p[i], 4);                  // one arrival per softmax warp
       mbar_init(&bar_pv[i], 1);
     }
     fence_mbar_init();
@@ -302,8 +301,11 @@ attn_fwd_f32_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
       for (int sb = wt; sb < 2 * G::NB; sb += NT)
         transpose_sub<HS>(smem + L::V_OFF + st * G::TILE_S, smem + L::VT_OFF + st2 * G::TILE_S, sb, lane);
       fence_proxy_async_smem();
-      mbar_arrive(&bar_vt_full[st2]);
-      if (j + ST < n_max) mbar_arrive(&bar_kv_empty[st]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bar_vt_full[st2]);
+        if (j + ST < n_max) mbar_arrive(&bar_kv_empty[st]);
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
@@ -380,7 +382,8 @@ attn_fwd_f32_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
       m_run = m_new;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar_p[wg]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p[wg]);
     }
     // every thread of the warpgroup takes the same branch at the barriers below
     ok = !named_bar_red_or(1 + wg, 128, !ok);
@@ -507,15 +510,15 @@ attn_bwd_dkdv_f32(const __grid_constant__ CUtensorMap map_kv, const __grid_const
     mbar_init(&bar_kv, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&bar_q_full[s], 1);
-      mbar_init(&bar_q_empty[s], 1 + NT_THREADS);    // the S^T/dP^T MMAs and the transposers
+      mbar_init(&bar_q_empty[s], 1 + NT);            // the S^T/dP^T MMAs and the transposer warps
     }
     for (int s = 0; s < ST2; ++s) {
-      mbar_init(&bar_qt_full[s], NT_THREADS);
+      mbar_init(&bar_qt_full[s], NT);
       mbar_init(&bar_qt_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_sdp[i], 1);
-      mbar_init(&bar_pds[i], 128);
+      mbar_init(&bar_pds[i], 4);                // one arrival per warp
       mbar_init(&bar_acc[i], 1);
     }
     mbar_init(&bar_done, 1);
@@ -620,8 +623,11 @@ attn_bwd_dkdv_f32(const __grid_constant__ CUtensorMap map_kv, const __grid_const
                           smem + (is_do ? L::DOT_OFF : L::QT_OFF) + st2 * G::TILE_S, x, lane);
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bar_qt_full[st2]);
-      if (i + ST < n_q) mbar_arrive(&bar_q_empty[st]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bar_qt_full[st2]);
+        if (i + ST < n_q) mbar_arrive(&bar_q_empty[st]);
+      }
     }
   } else {
     // ------------------------------------------------------------ P^T / dS^T warpgroup (thread = key row)
@@ -681,7 +687,8 @@ attn_bwd_dkdv_f32(const __grid_constant__ CUtensorMap map_kv, const __grid_const
       tmem_st32(tmem + lane_off + 128 + bb * 64 + 32, dp[1]);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar_pds[bb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_pds[bb]);
     }
     ok = !named_bar_red_or(1, 128, !ok);
     if (ok) {
@@ -768,15 +775,15 @@ attn_bwd_dq_f32(const __grid_constant__ CUtensorMap map_ql, const __grid_constan
     mbar_init(&bar_q, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&bar_kv_full[s], 1);
-      mbar_init(&bar_kv_empty[s], 1 + NT_THREADS);   // the S/dP MMAs and the transposers
+      mbar_init(&bar_kv_empty[s], 1 + NT);           // the S/dP MMAs and the transposer warps
     }
     for (int s = 0; s < ST2; ++s) {
-      mbar_init(&bar_kt_full[s], NT_THREADS);
+      mbar_init(&bar_kt_full[s], NT);
       mbar_init(&bar_kt_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_sdp[i], 1);
-      mbar_init(&bar_pds[i], 128);
+      mbar_init(&bar_pds[i], 4);                // one arrival per warp
       mbar_init(&bar_acc[i], 1);
     }
     mbar_init(&bar_done, 1);
@@ -868,8 +875,11 @@ attn_bwd_dq_f32(const __grid_constant__ CUtensorMap map_ql, const __grid_constan
       for (int sb = wt; sb < 2 * G::NB; sb += NT)
         transpose_sub<HS>(smem + L::K_OFF + st * G::TILE_S, smem + L::KT_OFF + st2 * G::TILE_S, sb, lane);
       fence_proxy_async_smem();
-      mbar_arrive(&bar_kt_full[st2]);
-      if (j + ST < n_k) mbar_arrive(&bar_kv_empty[st]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bar_kt_full[st2]);
+        if (j + ST < n_k) mbar_arrive(&bar_kv_empty[st]);
+      }
     }
   } else {
     // ------------------------------------------------------------ dS warpgroup (thread = query row)
@@ -907,7 +917,8 @@ attn_bwd_dq_f32(const __grid_constant__ CUtensorMap map_ql, const __grid_constan
       tmem_st32(tmem + lane_off + 128 + bb * 64 + 32, dp[1]);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar_pds[bb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_pds[bb]);
     }
     ok = !named_bar_red_or(1, 128, !ok);
     if (ok) {

@@ -122,8 +122,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_s[i], 1);
-      mbar_init(&bar_sfree[i], 128);
-      mbar_init(&bar_p[i], 128);
+      mbar_init(&bar_sfree[i], 4);               // one arrival per softmax warp
+      mbar_init(&bar_p[i], 4);
       mbar_init(&bar_pv[i], 1);
     }
     fence_mbar_init();
@@ -273,7 +273,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
         tmem_tie32(s[2]);
         tmem_tie32(s[3]);
         tc_fence_before();
-        mbar_arrive(&bar_sfree[wg]);                     // S columns may be overwritten now
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_sfree[wg]);      // S columns may be overwritten now
         // mask: causal diagonal tile (key > row), or keys past T (non-causal tail)
         const int kbase = j * BN;
         int limit = BN;                                  // keys [kbase, kbase+limit) are visible
@@ -343,7 +344,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
         m_run = m_new;
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bar_p[wg]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_p[wg]);
       }
       if (!ok) break;
       // -------------------------------------------------------- epilogue of this item
