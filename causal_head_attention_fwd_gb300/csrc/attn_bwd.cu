@@ -419,24 +419,25 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
           // bounded wait that gave up never leaves a thread stuck at a barrier
           const bool fail = !mbar_wait(&bar_dq_full, g & 1, &abort_sh, gerr);
           tc_fence_after();
-          uint32_t a[HS / 32][32];
-#pragma unroll
-          for (int cc = 0; cc < HS / 32; ++cc) tmem_ld32(tmem + lane_off + TB_DQ + cc * 32, a[cc]);
-          tmem_ld_wait(a[0]);
-          if constexpr (HS == 64) tmem_tie32(a[HS / 32 - 1]);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar_dq_free);
-          // one 32-column block at a time through the 16 KB staging tile
+          // one 32-column block at a time: TMEM -> 16 KB staging tile -> reduce;
+          // the dQ columns are released once the last block is in registers
 #pragma unroll
           for (int cc = 0; cc < HS / 32; ++cc) {
+            uint32_t a[32];
+            tmem_ld32(tmem + lane_off + TB_DQ + cc * 32, a);
+            tmem_ld_wait(a);
+            if (cc == HS / 32 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bar_dq_free);
+            }
             // the previous bulk operation must have finished reading the staging tile
             if (leader) bulk_wait_group_read0();
             if (named_bar_red_or(1, 128, fail)) { ok = false; break; }
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {           // [128 q][32 fp32], 128-byte swizzle
-              const float4 v = make_float4(__uint_as_float(a[cc][ch * 4 + 0]) * s, __uint_as_float(a[cc][ch * 4 + 1]) * s,
-                                           __uint_as_float(a[cc][ch * 4 + 2]) * s, __uint_as_float(a[cc][ch * 4 + 3]) * s);
+              const float4 v = make_float4(__uint_as_float(a[ch * 4 + 0]) * s, __uint_as_float(a[ch * 4 + 1]) * s,
+                                           __uint_as_float(a[ch * 4 + 2]) * s, __uint_as_float(a[ch * 4 + 3]) * s);
               *reinterpret_cast<float4*>(sdq + swz_chunk_offset<64>(r, ch)) = v;
             }
             fence_proxy_async_smem();

@@ -18,7 +18,7 @@
 //   warps 4-7  softmax warpgroup for query tile 1
 //   warp  8    TMA producer: Q (double-buffered per item), K/V tiles through
 //              a 3-stage ring that runs on across items
-//   warp  9    MMA issuer (single thread)
+//   warps 9-10 MMA issuers, one thread per query tile
 // S_i(j+1) is issued as soon as the softmax warps of tile i hold S_i(j) in
 // registers, so the next scores are ready when the softmax of this tile ends.
 // Each warpgroup writes its output tile through its own (then dead) Q tile and
@@ -30,7 +30,7 @@
 namespace attn {
 
 constexpr int FWD_STAGES = 3;
-constexpr int FWD_THREADS = 320;
+constexpr int FWD_THREADS = 352;
 constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 320, TM_P0 = 384, TM_P1 = 448;
 
 template <int HS>
@@ -118,7 +118,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
     for (int s = 0; s < FWD_STAGES; ++s) {
       mbar_init(&bar_k_full[s], 1);
       mbar_init(&bar_v_full[s], 1);
-      mbar_init(&bar_kv_empty[s], 1);
+      mbar_init(&bar_kv_empty[s], 2);            // one release per MMA issuer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_s[i], 1);
@@ -167,75 +167,71 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
         }
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers, one per query tile
+    // Each tile has its own issuing thread, so S_i(j+1) is issued as soon as
+    // softmax warpgroup i holds S_i(j), whatever the other tile is doing.
     if (lane == 0) {
+      const int i = warp - 9;                     // query tile of this issuer
       constexpr uint32_t idesc_s = make_idesc_bf16(BM, BN, false, false);
       constexpr uint32_t idesc_o = make_idesc_bf16(BM, HS, false, true);
       const uint64_t dQ0 = make_sdesc(smem_u32(smem + L::Q_OFF), 16, G::ATOM_BYTES, G::SWZ);
       const uint64_t dK0 = make_sdesc(smem_u32(smem + L::K_OFF), 16, G::ATOM_BYTES, G::SWZ);
       const uint64_t dV0 = make_sdesc(smem_u32(smem + L::V_OFF), 16, G::ATOM_BYTES, G::SWZ);
+      const uint32_t tS = tmem + (i ? TM_S1 : TM_S0), tO = tmem + (i ? TM_O1 : TM_O0), tP = tmem + (i ? TM_P1 : TM_P0);
       // S_i = Q_i K^T : K = HS in steps of 16 (32 bytes inside the swizzle row)
-      auto issue_s = [&](int i, int qb, int st) {
+      auto issue_s = [&](int qb, int st) {
         const uint64_t qd = desc_add(dQ0, (2 * qb + i) * G::TILE_BYTES), kd = desc_add(dK0, st * G::TILE_BYTES);
-        const uint32_t d = tmem + (i ? TM_S1 : TM_S0);
 #pragma unroll
-        for (int k = 0; k < HS / 16; ++k) mma_ss(d, desc_add(qd, k * 32), desc_add(kd, k * 32), idesc_s, k > 0);
+        for (int k = 0; k < HS / 16; ++k) mma_ss(tS, desc_add(qd, k * 32), desc_add(kd, k * 32), idesc_s, k > 0);
         mma_commit(&bar_s[i]);
       };
       // O_i += P_i V : K = 128 keys in steps of 16 (16 rows of V = 2 atoms)
-      auto issue_pv = [&](int i, int st, bool acc) {
+      auto issue_pv = [&](int st, bool acc) {
         const uint64_t vd = desc_add(dV0, st * G::TILE_BYTES);
-        const uint32_t d = tmem + (i ? TM_O1 : TM_O0), a = tmem + (i ? TM_P1 : TM_P0);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          mma_ts(d, a + k * 8, desc_add(vd, k * 16 * G::ROW_BYTES), idesc_o, (acc || k > 0) ? 1u : 0u);
+          mma_ts(tO, tP + k * 8, desc_add(vd, k * 16 * G::ROW_BYTES), idesc_o, (acc || k > 0) ? 1u : 0u);
         mma_commit(&bar_pv[i]);
       };
       bool ok = true;
       int gk = 0;                                 // key-tile steps so far
-      int gs[2] = {0, 0};                         // softmax steps of each query tile so far
+      int gs = 0;                                 // softmax steps of this query tile so far
       for (int ic = 0; ok && ic < n_items_cta; ++ic) {
         const FwdItem w = fwd_decode<CAUSAL>(fwd_item(ic), p);
         const int qb = ic & 1;
-        if (!(ok = mbar_wait(&bar_q_full[qb], (ic >> 1) & 1, &abort_sh, gerr))) break;
-        if (!(ok = mbar_wait(&bar_k_full[gk % FWD_STAGES], (gk / FWD_STAGES) & 1, &abort_sh, gerr))) break;
+        const int n = w.n_tile[i];
         // first scores of the item, once the softmax warps hold the previous S_i
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (w.n_tile[i] == 0) continue;
-          if (gs[i] > 0 && !(ok = mbar_wait(&bar_sfree[i], (gs[i] - 1) & 1, &abort_sh, gerr))) break;
+        if (n > 0) {
+          if (!(ok = mbar_wait(&bar_q_full[qb], (ic >> 1) & 1, &abort_sh, gerr))) break;
+          if (!(ok = mbar_wait(&bar_k_full[gk % FWD_STAGES], (gk / FWD_STAGES) & 1, &abort_sh, gerr))) break;
+          if (gs > 0 && !(ok = mbar_wait(&bar_sfree[i], (gs - 1) & 1, &abort_sh, gerr))) break;
           tc_fence_after();
-          issue_s(i, qb, gk % FWD_STAGES);
+          issue_s(qb, gk % FWD_STAGES);
         }
-        // per key tile j: S_i(j+1) for each query tile, then O_i += P_i(j) V_j
+        // per key tile j: S_i(j+1), then O_i += P_i(j) V_j
         for (int j = 0; ok && j < w.n_max; ++j) {
           const int st = (gk + j) % FWD_STAGES;
           const int st1 = (gk + j + 1) % FWD_STAGES;
-          bool k_ready = false;
-          for (int i = 0; i < 2 && ok; ++i) {
-            if (j + 1 >= w.n_tile[i]) continue;
-            if (!(ok = mbar_wait(&bar_sfree[i], (gs[i] + j) & 1, &abort_sh, gerr))) break;
-            if (!k_ready) {
-              if (!(ok = mbar_wait(&bar_k_full[st1], ((gk + j + 1) / FWD_STAGES) & 1, &abort_sh, gerr))) break;
-              k_ready = true;
-            }
+          if (j + 1 < n) {
+            if (!(ok = mbar_wait(&bar_sfree[i], (gs + j) & 1, &abort_sh, gerr))) break;
+            if (!(ok = mbar_wait(&bar_k_full[st1], ((gk + j + 1) / FWD_STAGES) & 1, &abort_sh, gerr))) break;
             tc_fence_after();
-            issue_s(i, qb, st1);
+            issue_s(qb, st1);
           }
-          if (!ok) break;
+          // every step, active or not, so this issuer never runs ahead of the
+          // producer (the K/V stage release below needs both issuers)
           if (!(ok = mbar_wait(&bar_v_full[st], ((gk + j) / FWD_STAGES) & 1, &abort_sh, gerr))) break;
-          for (int i = 0; i < 2 && ok; ++i) {
-            if (j >= w.n_tile[i]) continue;
-            if (!(ok = mbar_wait(&bar_p[i], (gs[i] + j) & 1, &abort_sh, gerr))) break;
+          if (j < n) {
+            if (!(ok = mbar_wait(&bar_p[i], (gs + j) & 1, &abort_sh, gerr))) break;
             tc_fence_after();
-            issue_pv(i, st, j > 0);
+            issue_pv(st, j > 0);
           }
           // release the K/V stage only if the producer will refill it (every
           // commit issued is awaited, so no arrival lands after the CTA retires)
-          if (ok && gk + j + FWD_STAGES < total_kv) mma_commit(&bar_kv_empty[st]);
+          if (gk + j + FWD_STAGES < total_kv) mma_commit(&bar_kv_empty[st]);
         }
-        gs[0] += w.n_tile[0];
-        gs[1] += w.n_tile[1];
+        gs += n;
         gk += w.n_max;
       }
     }
