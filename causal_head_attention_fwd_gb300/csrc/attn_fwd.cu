@@ -18,7 +18,8 @@
 //   warps 4-7  softmax warpgroup for query tile 1
 //   warp  8    TMA producer: Q (double-buffered per item), K/V tiles through
 //              a 3-stage ring that runs on across items
-//   warps 9-10 MMA issuers, one thread per query tile
+//   warps 9-10 MMA issuers, one thread per query tile; warp 11 idle
+//   (setmaxnreg: 208 registers for the softmax warpgroups, 80 for warps 8-11)
 // S_i(j+1) is issued as soon as the softmax warps of tile i hold S_i(j) in
 // registers, so the next scores are ready when the softmax of this tile ends.
 // Each warpgroup writes its output tile through its own (then dead) Q tile and
@@ -30,7 +31,10 @@
 namespace attn {
 
 constexpr int FWD_STAGES = 3;
-constexpr int FWD_THREADS = 352;
+constexpr int FWD_THREADS = 384;
+// register split: the two softmax warpgroups up, the producer/MMA warpgroup down
+constexpr uint32_t FREG_SOFTMAX = 208, FREG_OTHER = 80;
+static_assert(256 * FREG_SOFTMAX + 128 * FREG_OTHER <= 384 * 168, "register split exceeds the pool");
 constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 320, TM_P0 = 384, TM_P1 = 448;
 
 template <int HS>
@@ -138,6 +142,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
   const uint32_t tmem = tmem_base_sh;
   int* gerr = p.err;
 
+  if (warp >= 8) {
+  setmaxnreg_dec<FREG_OTHER>();
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -235,7 +241,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
         gk += w.n_max;
       }
     }
+  }                                             // warp 11 only donates registers
   } else {
+    setmaxnreg_inc<FREG_SOFTMAX>();
     // ------------------------------------------------------------ softmax warpgroups
     const int wg = warp >> 2;                    // query tile index 0/1
     const int r = ((warp & 3) << 5) + lane;      // row inside the tile = TMEM lane
