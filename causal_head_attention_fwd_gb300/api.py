@@ -27,7 +27,7 @@ ATTN_BF16 = 1
 
 EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_status_string",
             "attn_last_device_error", "attn_profile_enable", "attn_profile_reset",
-            "attn_profile_read", "attn_bwd_noalloc")
+            "attn_profile_read", "attn_bwd_noalloc", "attn_selftest_wait_timeout")
 
 # size of the fixed scratch array attn_bwd_noalloc uses (ATTN_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -72,6 +72,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_profile_read.restype = i
     lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, f_p, vp, i, i, i, i, i, i, vp]
     lib.attn_bwd_noalloc.restype = i
+    lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+    lib.attn_selftest_wait_timeout.restype = i
     return lib
 
 
@@ -138,6 +140,10 @@ def attn_bwd(dout, qkv, out, lse, dqkv, B, T, C, NH, causal, dtype, workspace, w
 
 def attn_last_device_error(stream=None) -> int:
     return int(_lib.attn_last_device_error(_stream(stream)))
+
+
+def attn_selftest_wait_timeout(limit_us: int, stream=None) -> int:
+    return int(_lib.attn_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def attn_profile_enable(enable: bool) -> None:

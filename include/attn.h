@@ -121,6 +121,18 @@ attn_status_t attn_bwd_noalloc(const void* dout, const void* qkv, const void* ou
                                attn_dtype_t dtype, void* stream);
 
 /*
+ * Failure-detection self-test (no counterpart on the pages). Launches one warp
+ * that waits, with the bounded-wait mechanism every kernel of this library
+ * uses, on an mbarrier phase nothing completes; after limit_us microseconds
+ * (1 .. 10^7) it records ATTN_ERR_TIMEOUT in the device error word and returns.
+ * The GPU is never faulted or hung: the next attn_last_device_error on the
+ * stream returns ATTN_ERR_TIMEOUT (and clears the word), and later calls work
+ * normally. Returns ATTN_ERR_INVALID_ARG for a limit out of range, else the
+ * launch status.
+ */
+attn_status_t attn_selftest_wait_timeout(unsigned int limit_us, void* stream);
+
+/*
  * Per-kernel timing (diagnostics; no counterpart on the pages beyond llm.c's
  * benchmark timing loop). While enabled, every kernel the library launches is
  * bracketed by two CUDA events recorded on its stream; attn_profile_read
