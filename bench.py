@@ -214,6 +214,54 @@ def config_dict(w):
             "l2": "flushed between timed steps (512 MiB write)"}
 
 
+# ----------------------------------------------------------------------------- llm.c drop-in mode
+def run_att(args):
+    """Times attn_fwd_att (preatt and att materialised, fp32 B x NH x T x T) on
+    one GPU. Bound by the HBM writes of the two matrices."""
+    import torch
+    from causal_head_attention_fwd_gb300 import build, inputs
+    build.build()
+    from causal_head_attention_fwd_gb300 import api, ops
+    dev = torch.device("cuda", 0)
+    w = inputs.WORKLOADS[args.workload]
+    B, T, C, NH, causal = w.B, w.T, w.C, w.NH, w.causal
+    host = inputs.make_inputs(B, T, C, NH, w.dtype, w.sigma_qkv, w.sigma_dout, w.seed_qkv, w.seed_dout)
+    qkv = ops.upload(host.qkv_dev, w.dtype, dev)
+    out, lse = ops.attention_forward(qkv, NH, bool(causal))
+    pre = torch.empty((B, NH, T, T), dtype=torch.float32, device=dev)
+    att = torch.empty_like(pre)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        ops.attention_matrices(qkv, lse, NH, bool(causal), preatt=pre, att=att, stream=stream)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(0) as cs:
+        for a, b in ev:
+            flush.fill_(1.0)
+            a.record(stream)
+            ops.attention_matrices(qkv, lse, NH, bool(causal), preatt=pre, att=att, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+    if api.attn_last_device_error(stream) != api.ATTN_OK:
+        raise RuntimeError("device error in the timed region")
+    t_ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    esz = 2 if w.dtype == "bf16" else 4
+    nbytes = 2 * B * NH * T * T * 4 + B * T * 2 * C * esz + B * NH * T * 4   # writes + q,k + lse reads
+    peaks, src = load_peaks()
+    gbs = nbytes / (t_ms * 1e-3) / 1e9
+    line = {"metric": "llm.c drop-in attention matrices (preatt + att) GB/s at 1 GB300", "value": gbs,
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic", "config": config_dict(w),
+            "roofline": {"kernel": "attn_att_kernel", "bound": "hbm", "achieved": gbs,
+                         "peak": float(peaks["hbm_gbs"]), "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]),
+                         "traffic": None, "peak_source": f"{src} HBM copy (MEASURED_PEAKS.json hbm_gbs)"},
+            "bytes_per_step": nbytes, "gpu_launches": args.steps, "clocks": cs.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def main(argv=None):
     ap = argparse.ArgumentParser()
@@ -223,11 +271,16 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--att", action="store_true",
+                    help="time the llm.c drop-in mode (attn_fwd_att: preatt and att, B x NH x T x T fp32) "
+                         "instead of the fwd+bwd step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.att:
+        return run_att(args)
 
     import numpy as np
     import torch

@@ -27,7 +27,7 @@ ATTN_BF16 = 1
 
 EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_status_string",
             "attn_last_device_error", "attn_profile_enable", "attn_profile_reset",
-            "attn_profile_read", "attn_bwd_noalloc", "attn_selftest_wait_timeout")
+            "attn_profile_read", "attn_bwd_noalloc", "attn_selftest_wait_timeout", "attn_fwd_att")
 
 # size of the fixed scratch array attn_bwd_noalloc uses (ATTN_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -74,6 +74,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_bwd_noalloc.restype = i
     lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
     lib.attn_selftest_wait_timeout.restype = i
+    lib.attn_fwd_att.argtypes = [vp, f_p, f_p, f_p, i, i, i, i, i, i, vp]
+    lib.attn_fwd_att.restype = i
     return lib
 
 
@@ -140,6 +142,14 @@ def attn_bwd(dout, qkv, out, lse, dqkv, B, T, C, NH, causal, dtype, workspace, w
 
 def attn_last_device_error(stream=None) -> int:
     return int(_lib.attn_last_device_error(_stream(stream)))
+
+
+def attn_fwd_att(qkv, lse, preatt, att, B, T, C, NH, causal, dtype, stream=None, check=True) -> int:
+    st = _lib.attn_fwd_att(_ptr(qkv), _ptr(lse), _ptr(preatt), _ptr(att), B, T, C, NH, int(causal),
+                           _dtype(dtype), _stream(stream))
+    if check and st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_att")
+    return st
 
 
 def attn_selftest_wait_timeout(limit_us: int, stream=None) -> int:

@@ -29,6 +29,9 @@ cudaError_t launch_bwd_f32(const CUtensorMap& map_q_l, const CUtensorMap& map_q_
                            const float* out, const float* lse, float* ws_D, const Problem& pr,
                            cudaStream_t stream);
 
+cudaError_t launch_att(const CUtensorMap& map_qkv, const float* lse, float* preatt, float* att, bool f32,
+                       const Problem& pr, cudaStream_t stream);
+
 static __device__ int g_error_word = 0;
 
 static constexpr int kMaxDevices = 64;
@@ -273,6 +276,34 @@ extern "C" attn_status_t attn_bwd(const void* dout, const void* qkv, const void*
     return ATTN_ERR_CUDA;
   cudaError_t ce = launch_bwd_bf16(mq, md, mg, ma, dout, out, lse, dqkv, ws_D, ws_dq, pr,
                                    static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" attn_status_t attn_fwd_att(const void* qkv, const float* lse, float* preatt, float* att, int B, int T,
+                                      int C, int NH, int causal, attn_dtype_t dtype, void* stream) {
+  attn_status_t st = check_shape(B, T, C, NH, causal, dtype);
+  if (st != ATTN_OK) return st;
+  if (!qkv || !lse || (!preatt && !att)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(lse) || (preatt && !aligned16(preatt)) || (att && !aligned16(att)))
+    return ATTN_ERR_MISALIGNED;
+  const long long nt = (T + 127) / 128;
+  if ((double)B * NH * (double)nt * (double)nt > 2.0e9) return ATTN_ERR_INVALID_ARG;
+  const size_t e = esize(dtype);
+  const size_t nq = (size_t)B * T * 3 * C * e, nl = (size_t)B * NH * T * 4, na = (size_t)B * NH * T * (size_t)T * 4;
+  if ((preatt && (overlaps(preatt, na, qkv, nq) || overlaps(preatt, na, lse, nl))) ||
+      (att && (overlaps(att, na, qkv, nq) || overlaps(att, na, lse, nl))) ||
+      (preatt && att && overlaps(preatt, na, att, na)))
+    return ATTN_ERR_INVALID_ARG;
+  Problem pr{B, T, C, NH, C / NH, causal};
+  if (!device_error_word()) return ATTN_ERR_CUDA;
+  CUtensorMap mq;
+  const bool f32 = dtype == ATTN_F32;
+  const bool enc = f32 ? encode_3d(&mq, qkv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 3 * C, T, B, 32, BM,
+                                   CU_TENSOR_MAP_SWIZZLE_128B)
+                       : encode_3d(&mq, qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3 * C, T, B, pr.hs, BM,
+                                   pr.hs == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!enc) return ATTN_ERR_CUDA;
+  cudaError_t ce = launch_att(mq, lse, preatt, att, f32, pr, static_cast<cudaStream_t>(stream));
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -53,6 +53,20 @@ def attention_forward(qkv: torch.Tensor, n_head: int, causal: bool = True, out=N
     return out, lse
 
 
+def attention_matrices(qkv: torch.Tensor, lse: torch.Tensor, n_head: int, causal: bool = True,
+                       preatt=True, att=True, stream=None):
+    """llm.c drop-in mode: (preatt, att), each (B, NH, T, T) fp32 or None.
+    preatt = q.k without the scale (full matrix); att = the softmax with the
+    masked entries set to zero. lse is the forward's row statistic."""
+    B, T, C, NH = _shape(qkv, n_head)
+    pa = torch.empty((B, NH, T, T), dtype=torch.float32, device=qkv.device) if preatt is True else preatt
+    at = torch.empty((B, NH, T, T), dtype=torch.float32, device=qkv.device) if att is True else att
+    pa = pa if pa is not False else None
+    at = at if at is not False else None
+    api.attn_fwd_att(qkv, lse, pa, at, B, T, C, NH, int(causal), _DT[qkv.dtype], stream)
+    return pa, at
+
+
 class Workspace:
     """Reusable device scratch buffer for attn_bwd (grown on demand)."""
 

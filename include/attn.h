@@ -85,6 +85,24 @@ attn_status_t attn_bwd(const void* dout, const void* qkv, const void* out, const
                        void* dqkv, int B, int T, int C, int NH, int causal, attn_dtype_t dtype,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * llm.c drop-in mode: materialise the forward's attention matrices, as llm.c's
+ * attention_forward keeps them (dev/cuda/attention_backward.cu), for debugging
+ * and for code that consumes them. Needs the lse attn_fwd wrote for the same
+ * qkv. Either output may be NULL to skip it.
+ *   qkv    : (B, T, 3C) dtype, read only.
+ *   lse    : (B, NH, T) fp32 from attn_fwd, read only.
+ *   preatt : (B, NH, T, T) fp32, q_t . k_j without the scale, every (t, j),
+ *            the masked part included (as llm.c materialises it).
+ *   att    : (B, NH, T, T) fp32, exp(scale * preatt - lse_t) on the visible
+ *            keys J(t), 0 elsewhere (the masked entries are written as zero).
+ * The T x T products run on the tensor core (bf16: bf16 products; fp32: tf32
+ * products), fp32 accumulation. Buffers 16-byte aligned, no overlaps;
+ * ATTN_ERR_INVALID_ARG if B*NH*ceil(T/128)^2 exceeds 2e9.
+ */
+attn_status_t attn_fwd_att(const void* qkv, const float* lse, float* preatt, float* att, int B, int T, int C,
+                           int NH, int causal, attn_dtype_t dtype, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* attn_status_string(attn_status_t status);
 

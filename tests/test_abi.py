@@ -109,3 +109,16 @@ def test_product_path_has_no_oracle_or_fallback():
         src = f.read_text()
         assert "import oracle" not in src and "from oracle" not in src, f
     assert "raise ImportError" in (pkg / "api.py").read_text()
+
+
+def test_att_rejects_bad_arguments(api):
+    ok = dict(qkv=A, lse=A + S, pre=A + 2 * S, att=A + 3 * S)
+    def call(**kw):
+        a = dict(ok, **kw)
+        return api.attn_fwd_att(a["qkv"], a["lse"], a["pre"], a["att"], 2, 64, 128, 2, 1, 1, 0, check=False)
+    assert call(qkv=0) == api.ATTN_ERR_INVALID_ARG
+    assert call(pre=0, att=0) == api.ATTN_ERR_INVALID_ARG
+    assert call(att=A + 3 * S + 4) == api.ATTN_ERR_MISALIGNED
+    assert call(att=A + 2 * S) == api.ATTN_ERR_INVALID_ARG        # preatt and att overlap
+    assert api.attn_fwd_att(A, A + S, A + 2 * S, None, 2, 64, 96, 2, 1, 1, 0, check=False) == \
+        api.ATTN_ERR_UNSUPPORTED                                    # hs = 48
