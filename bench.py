@@ -262,6 +262,66 @@ def run_att(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- decode forward
+def run_decode(args):
+    """Times attn_decode (the last Tq tokens of each sequence against its whole
+    key/value cache). Bound by reading the cache from HBM."""
+    import torch
+    from causal_head_attention_fwd_gb300 import build, inputs
+    build.build()
+    from causal_head_attention_fwd_gb300 import api, ops
+    dev = torch.device("cuda", 0)
+    w = inputs.DECODE_WORKLOADS[args.decode]
+    B, L, C, NH, Tq = w.B, w.L, w.C, w.NH, w.Tq
+    _, qkv_dev = inputs.draw((B, L, 3 * C), w.sigma_qkv, w.seed_qkv, w.dtype)
+    qkv = ops.upload(qkv_dev, w.dtype, dev)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    out = torch.empty((B, Tq, C), dtype=tdt, device=dev)
+    lse = torch.empty((B, NH, Tq), dtype=torch.float32, device=dev)
+    adt = api.ATTN_BF16 if w.dtype == "bf16" else api.ATTN_F32
+    nws = api.attn_decode_workspace_size(B, L, C, NH, Tq, adt)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        api.attn_decode(qkv, out, lse, B, L, C, NH, Tq, adt, ws, nws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(0) as cs:
+        for a, b in ev:
+            flush.fill_(1.0)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+    if api.attn_last_device_error(stream) != api.ATTN_OK:
+        raise RuntimeError("device error in the timed region")
+    t_ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    esz = 2 if w.dtype == "bf16" else 4
+    cache = 2 * B * L * C * esz                                   # K and V of every position
+    nbytes = cache + B * Tq * C * esz * 2 + 2 * nws + B * NH * Tq * 4
+    peaks, src = load_peaks()
+    gbs = nbytes / (t_ms * 1e-3) / 1e9
+    line = {"metric": "decode forward (KV-cache stream) GB/s at 1 GB300", "value": gbs, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic",
+            "config": {"workload": f"{w.name}: B={B} cached L={L} new Tq={Tq} C={C} NH={NH} hs={w.hs}, {w.dtype}",
+                       "B": B, "L": L, "Tq": Tq, "C": C, "NH": NH,
+                       "l2": "flushed between timed steps (512 MiB write)"},
+            "roofline": {"kernel": "attn_decode_split", "bound": "hbm", "achieved": gbs,
+                         "peak": float(peaks["hbm_gbs"]), "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]),
+                         "traffic": None, "peak_source": f"{src} HBM copy (MEASURED_PEAKS.json hbm_gbs)"},
+            "bytes_per_step": nbytes, "cache_bytes": cache, "tokens_per_s": B * Tq / (t_ms * 1e-3),
+            "gpu_launches": 2 * args.steps, "clocks": cs.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def main(argv=None):
     ap = argparse.ArgumentParser()
@@ -271,6 +331,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--decode", default=None, metavar="NAME",
+                    help="time the decode forward (attn_decode) on a decode workload, e.g. gpt2s_decode")
     ap.add_argument("--att", action="store_true",
                     help="time the llm.c drop-in mode (attn_fwd_att: preatt and att, B x NH x T x T fp32) "
                          "instead of the fwd+bwd step")
@@ -281,6 +343,8 @@ def main(argv=None):
         return run_reference(args)
     if args.att:
         return run_att(args)
+    if args.decode:
+        return run_decode(args)
 
     import numpy as np
     import torch

@@ -27,7 +27,8 @@ ATTN_BF16 = 1
 
 EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_status_string",
             "attn_last_device_error", "attn_profile_enable", "attn_profile_reset",
-            "attn_profile_read", "attn_bwd_noalloc", "attn_selftest_wait_timeout", "attn_fwd_att")
+            "attn_profile_read", "attn_bwd_noalloc", "attn_selftest_wait_timeout", "attn_fwd_att",
+            "attn_decode_workspace_size", "attn_decode")
 
 # size of the fixed scratch array attn_bwd_noalloc uses (ATTN_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -76,6 +77,10 @@ def _load() -> ctypes.CDLL:
     lib.attn_selftest_wait_timeout.restype = i
     lib.attn_fwd_att.argtypes = [vp, f_p, f_p, f_p, i, i, i, i, i, i, vp]
     lib.attn_fwd_att.restype = i
+    lib.attn_decode_workspace_size.argtypes = [i, i, i, i, i, i]
+    lib.attn_decode_workspace_size.restype = sz
+    lib.attn_decode.argtypes = [vp, vp, f_p, i, i, i, i, i, i, vp, sz, vp]
+    lib.attn_decode.restype = i
     return lib
 
 
@@ -149,6 +154,19 @@ def attn_fwd_att(qkv, lse, preatt, att, B, T, C, NH, causal, dtype, stream=None,
                            _dtype(dtype), _stream(stream))
     if check and st != ATTN_OK:
         raise AttnError(st, "attn_fwd_att")
+    return st
+
+
+def attn_decode_workspace_size(B, L, C, NH, Tq, dtype) -> int:
+    return int(_lib.attn_decode_workspace_size(B, L, C, NH, Tq, _dtype(dtype)))
+
+
+def attn_decode(qkv, out, lse, B, L, C, NH, Tq, dtype, workspace, workspace_bytes, stream=None,
+                check=True) -> int:
+    st = _lib.attn_decode(_ptr(qkv), _ptr(out), _ptr(lse), B, L, C, NH, Tq, _dtype(dtype), _ptr(workspace),
+                          int(workspace_bytes), _stream(stream))
+    if check and st != ATTN_OK:
+        raise AttnError(st, "attn_decode")
     return st
 
 

@@ -32,6 +32,12 @@ cudaError_t launch_bwd_f32(const CUtensorMap& map_q_l, const CUtensorMap& map_q_
 cudaError_t launch_att(const CUtensorMap& map_qkv, const float* lse, float* preatt, float* att, bool f32,
                        const Problem& pr, cudaStream_t stream);
 
+size_t decode_workspace_bytes(int B, int L, int C, int NH, int Tq, bool f32);
+int decode_max_tq();
+int decode_chunk(bool f32);
+cudaError_t launch_decode(const CUtensorMap& map_qkv, const void* qkv, void* out, float* lse, float* part, bool f32,
+                          int B, int L, int C, int NH, int Tq, cudaStream_t stream);
+
 static __device__ int g_error_word = 0;
 
 static constexpr int kMaxDevices = 64;
@@ -304,6 +310,45 @@ extern "C" attn_status_t attn_fwd_att(const void* qkv, const float* lse, float* 
                                    pr.hs == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (!enc) return ATTN_ERR_CUDA;
   cudaError_t ce = launch_att(mq, lse, preatt, att, f32, pr, static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+static attn_status_t check_decode(int B, int L, int C, int NH, int Tq, attn_dtype_t dtype) {
+  attn_status_t st = check_shape(B, L, C, NH, 1, dtype);
+  if (st != ATTN_OK) return st;
+  if (Tq < 1 || Tq > L || Tq > decode_max_tq()) return ATTN_ERR_INVALID_ARG;
+  const int ch = decode_chunk(dtype == ATTN_F32);
+  if ((double)B * NH * ((L + ch - 1) / ch) > 2.0e9) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+extern "C" size_t attn_decode_workspace_size(int B, int L, int C, int NH, int Tq, attn_dtype_t dtype) {
+  if (check_decode(B, L, C, NH, Tq, dtype) != ATTN_OK) return 0;
+  return decode_workspace_bytes(B, L, C, NH, Tq, dtype == ATTN_F32);
+}
+
+extern "C" attn_status_t attn_decode(const void* qkv, void* out, float* lse, int B, int L, int C, int NH, int Tq,
+                                     attn_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  attn_status_t st = check_decode(B, L, C, NH, Tq, dtype);
+  if (st != ATTN_OK) return st;
+  if (!qkv || !out || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(out) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
+  const size_t need = decode_workspace_bytes(B, L, C, NH, Tq, dtype == ATTN_F32);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_MISALIGNED;
+  const size_t e = esize(dtype);
+  const size_t nq = (size_t)B * L * 3 * C * e, no = (size_t)B * Tq * C * e, nl = (size_t)B * NH * Tq * 4;
+  if (overlaps(out, no, qkv, nq) || overlaps(lse, nl, qkv, nq) || overlaps(lse, nl, out, no) ||
+      overlaps(workspace, need, qkv, nq) || overlaps(workspace, need, out, no) || overlaps(workspace, need, lse, nl))
+    return ATTN_ERR_INVALID_ARG;
+  if (!device_error_word()) return ATTN_ERR_CUDA;
+  const bool f32 = dtype == ATTN_F32;
+  CUtensorMap mq;
+  if (!encode_3d(&mq, qkv, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 ? 4 : 2,
+                 3 * C, L, B, C / NH, decode_chunk(f32), CU_TENSOR_MAP_SWIZZLE_NONE))
+    return ATTN_ERR_CUDA;
+  cudaError_t ce = launch_decode(mq, qkv, out, lse, static_cast<float*>(workspace), f32, B, L, C, NH, Tq,
+                                 static_cast<cudaStream_t>(stream));
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

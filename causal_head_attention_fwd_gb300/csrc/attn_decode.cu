@@ -1,0 +1,314 @@
+// Decode forward: a few new query tokens attending to a key/value cache.
+//
+// In autoregressive inference (the pages' inference setting, where a `step`
+// offset places the new tokens after the ones already processed) the newest
+// Tq tokens of each sequence attend to every key up to their own position.
+// The layout stays llm.c's: qkv is (B, L, 3C); its K and V slots for positions
+// 0..L-1 are the cache (the new tokens included), and the queries are the last
+// Tq rows. Query i sits at position p_i = L - Tq + i and sees keys 0..p_i:
+//   out[b,i,h*hs+d] = sum_{j<=p_i} softmax_j(scale * q_i . k_j) v_j[d]
+//   lse[b,h,i]      = logsumexp_{j<=p_i}(scale * q_i . k_j)
+// With Tq small the arithmetic is a few multiply-adds per byte of K and V, so
+// the work is a stream over the cache, bound by HBM bandwidth (kept off the
+// tensor core: reshaping it into an MMA would not move the bound):
+//   attn_decode_split   one CTA per (b, h, chunk of 128 keys):
+//                       the chunk's K and V rows arrive in shared memory by
+//                       two bulk tensor copies issued at the start (V lands
+//                       while the scores are formed); q in shared memory;
+//                       every row is read by hs/8 lanes, 8 elements each;
+//                       partial dot products summed across those lanes; a
+//                       chunk-local softmax (max, exp2, sum); the partial
+//                       output summed over the rows of a warp and the warps;
+//                       written as (m, l, o)
+//   attn_decode_combine one warp-pair per (b, h, i): merges the chunks'
+//                       partial results (log-sum-exp rescaling) into out, lse
+#include "../../include/attn.h"
+#include "common.cuh"
+
+namespace attn {
+namespace deck {
+
+constexpr int THREADS = 128;
+constexpr int MAX_TQ = 8;
+
+struct Params {
+  const void* qkv;
+  void* out;
+  float* lse;
+  float* part;                          // [B*NH][n_split][Tq][HS + 2]: m, l, o[HS]
+  int* err;
+  int L, C, NH, Tq, n_split;
+  float scale_log2;
+};
+
+template <typename E>
+__device__ __forceinline__ float ld_e(const E* p);
+template <>
+__device__ __forceinline__ float ld_e<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float ld_e<uint16_t>(const uint16_t* p) {
+  return __uint_as_float((uint32_t)(*p) << 16);
+}
+
+// Load 8 consecutive elements (16 bytes of bf16 or 2 x 16 bytes of fp32) as fp32.
+template <typename E>
+__device__ __forceinline__ void load8(const E* src, float (&x)[8]) {
+  if constexpr (sizeof(E) == 4) {
+    const float4 a = *reinterpret_cast<const float4*>(src);
+    const float4 c = *reinterpret_cast<const float4*>(src + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = c.x; x[5] = c.y; x[6] = c.z; x[7] = c.w;
+  } else {
+    const uint4 v = *reinterpret_cast<const uint4*>(src);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[2 * k] = __uint_as_float(w[k] << 16);
+      x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+}
+
+template <typename E>
+struct Chunk {
+  // keys per split CTA: the K and V rows of a chunk are staged in shared memory
+  static constexpr int N = 128;
+};
+
+template <typename E, int HS>
+__global__ void __launch_bounds__(THREADS)
+attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
+  // A K or V row (HS elements) is read by LPR lanes, 8 elements each, so a
+  // warp instruction covers whole rows; GROUPS rows at a time.
+  constexpr int CH = Chunk<E>::N;
+  constexpr int LPR = HS / 8;                 // lanes per row (8 for hs 64, 4 for hs 32)
+  constexpr int GROUPS = THREADS / LPR;       // rows per CTA step
+  constexpr uint32_t BYTES = CH * HS * sizeof(E);
+  extern __shared__ uint8_t smem_raw[];
+  E* sK = reinterpret_cast<E*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  E* sV = sK + CH * HS;
+  __shared__ __align__(16) float sq[MAX_TQ][HS];
+  __shared__ float sp[MAX_TQ][CH];
+  __shared__ float red[MAX_TQ][THREADS / 32];
+  __shared__ float row_m[MAX_TQ];
+  __shared__ float sacc[THREADS / 32][MAX_TQ][HS];
+  __shared__ uint64_t bar_k, bar_v;
+  __shared__ volatile int abort_sh;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int split = blockIdx.x % p.n_split;
+  const int bh = blockIdx.x / p.n_split;
+  const int b = bh / p.NH, h = bh % p.NH;
+  const int L = p.L, C = p.C, Tq = p.Tq;
+  const int j0 = split * CH;
+  const int nk = min(CH, L - j0);
+  const int g = tid / LPR, db = (tid % LPR) * 8;   // row group, first of this lane's 8 columns
+  // the whole chunk of K and of V, one bulk tensor copy each (rows past L read
+  // as zero); V lands while the scores and the softmax are computed
+  if (tid == 0) {
+    abort_sh = 0;
+    mbar_init(&bar_k, 1);
+    mbar_init(&bar_v, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar_k, BYTES);
+    tma_load_3d(sK, &map_qkv, &bar_k, C + h * HS, j0, b);
+    mbar_arrive_expect_tx(&bar_v, BYTES);
+    tma_load_3d(sV, &map_qkv, &bar_v, 2 * C + h * HS, j0, b);
+  }
+  // the queries (last Tq positions) into shared memory, fp32
+  const size_t rs = (size_t)3 * C;
+  const E* qbase = static_cast<const E*>(p.qkv) + (size_t)b * L * rs + h * HS;
+  for (int x = tid; x < Tq * LPR; x += THREADS) {
+    const int i = x / LPR, c = (x % LPR) * 8;
+    float v[8];
+    load8<E>(qbase + (size_t)(L - Tq + i) * rs + c, v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) sq[i][c + k] = v[k];
+  }
+  __syncthreads();
+  bool ok = mbar_wait(&bar_k, 0, &abort_sh, p.err);
+  // scores: partial dot products over 8 columns, summed over the row's lanes
+  for (int r0 = 0; r0 < CH; r0 += GROUPS) {
+    const int j = r0 + g;
+    float kv[8];
+    load8<E>(sK + j * HS + db, kv);
+    for (int i = 0; i < Tq; ++i) {
+      const float4 qa = *reinterpret_cast<const float4*>(&sq[i][db]);
+      const float4 qb = *reinterpret_cast<const float4*>(&sq[i][db + 4]);
+      float acc = qa.x * kv[0];
+      acc = fmaf(qa.y, kv[1], acc);
+      acc = fmaf(qa.z, kv[2], acc);
+      acc = fmaf(qa.w, kv[3], acc);
+      acc = fmaf(qb.x, kv[4], acc);
+      acc = fmaf(qb.y, kv[5], acc);
+      acc = fmaf(qb.z, kv[6], acc);
+      acc = fmaf(qb.w, kv[7], acc);
+#pragma unroll
+      for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if ((tid % LPR) == 0)
+        sp[i][j] = (j < nk && j0 + j <= L - Tq + i) ? acc * p.scale_log2 : -INFINITY;   // log2 units
+    }
+  }
+  __syncthreads();
+  // chunk-local softmax per query: max, then exp2 and sum
+  for (int i = 0; i < Tq; ++i) {
+    float m = -INFINITY;
+    for (int j = tid; j < CH; j += THREADS) m = fmaxf(m, sp[i][j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[i][warp] = m;
+  }
+  __syncthreads();
+  if (tid < Tq) {
+    float m = red[tid][0];
+#pragma unroll
+    for (int w = 1; w < THREADS / 32; ++w) m = fmaxf(m, red[tid][w]);
+    row_m[tid] = m;
+  }
+  __syncthreads();
+  for (int i = 0; i < Tq; ++i) {
+    const float m = row_m[i];
+    float l = 0.f;
+    for (int j = tid; j < CH; j += THREADS) {
+      const float e = m == -INFINITY ? 0.f : ex2_approx(sp[i][j] - m);
+      sp[i][j] = e;
+      l += e;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (lane == 0) red[i][warp] = l;
+  }
+  __syncthreads();
+  ok = mbar_wait(&bar_v, 0, &abort_sh, p.err) && ok;
+  // partial outputs: each lane accumulates its 8 columns over its rows of the
+  // chunk for every query, then the rows of a warp and the warps are summed
+  float acc[MAX_TQ][8];
+#pragma unroll
+  for (int i = 0; i < MAX_TQ; ++i)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[i][k] = 0.f;
+#pragma unroll 4
+  for (int r0 = 0; r0 < CH; r0 += GROUPS) {
+    const int j = r0 + g;
+    float vv[8];
+    load8<E>(sV + j * HS + db, vv);               // rows past L are zero, their p is 0
+#pragma unroll
+    for (int i = 0; i < MAX_TQ; ++i) {
+      if (i < Tq) {
+        const float pj = sp[i][j];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[i][k] = fmaf(pj, vv[k], acc[i][k]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < MAX_TQ; ++i) {
+    if (i < Tq) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float v = acc[i][k];
+#pragma unroll
+        for (int o = LPR; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);   // rows of the warp
+        acc[i][k] = v;
+      }
+      if (lane < LPR) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sacc[warp][i][db + k] = acc[i][k];
+      }
+    }
+  }
+  __syncthreads();
+  if (!ok) return;                                  // the error word says why
+  // partial record: m (log2 units), l, o[HS]
+  float* rec = p.part + ((size_t)bh * p.n_split + split) * Tq * (HS + 2);
+  for (int x = tid; x < Tq * HS; x += THREADS) {
+    const int i = x / HS, d = x % HS;
+    float o = 0.f;
+#pragma unroll
+    for (int w = 0; w < THREADS / 32; ++w) o += sacc[w][i][d];
+    rec[i * (HS + 2) + 2 + d] = o;
+  }
+  if (tid < Tq) {
+    float l = 0.f;
+#pragma unroll
+    for (int w = 0; w < THREADS / 32; ++w) l += red[tid][w];
+    rec[tid * (HS + 2) + 0] = row_m[tid];
+    rec[tid * (HS + 2) + 1] = l;
+  }
+}
+
+// One block of HS threads per (b, h, query): merge the chunks' partials.
+template <typename E, int HS>
+__global__ void __launch_bounds__(HS) attn_decode_combine(const Params p) {
+  const int i = blockIdx.x % p.Tq;
+  const int bh = blockIdx.x / p.Tq;
+  const int b = bh / p.NH, h = bh % p.NH;
+  const int d = threadIdx.x;
+  const int Tq = p.Tq;
+  // only chunks that hold a visible key of this query contribute
+  const int last = (p.L - Tq + i) / Chunk<E>::N;
+  const float* rec = p.part + (size_t)bh * p.n_split * Tq * (HS + 2) + i * (HS + 2);
+  float M = -INFINITY;
+  for (int s = 0; s <= last; ++s) M = fmaxf(M, rec[(size_t)s * Tq * (HS + 2)]);
+  float l = 0.f, o = 0.f;
+  for (int s = 0; s <= last; ++s) {
+    const float* r = rec + (size_t)s * Tq * (HS + 2);
+    const float w = ex2_approx(r[0] - M);
+    l = fmaf(r[1], w, l);
+    o = fmaf(r[2 + d], w, o);
+  }
+  const float val = o / l;
+  const size_t oi = ((size_t)b * Tq + i) * p.C + h * HS + d;
+  if constexpr (sizeof(E) == 4) static_cast<float*>(p.out)[oi] = val;
+  else static_cast<uint16_t*>(p.out)[oi] = (uint16_t)(pack_bf16x2(val, 0.f) & 0xFFFFu);
+  if (d == 0) p.lse[(size_t)bh * Tq + i] = (M + __log2f(l)) * 0.69314718055994531f;
+}
+
+template <typename E, int HS>
+static cudaError_t launch_t(const CUtensorMap& m, const Params& p, int BH, cudaStream_t s) {
+  constexpr int SMEM = 2 * Chunk<E>::N * HS * (int)sizeof(E) + 128;
+  auto k = attn_decode_split<E, HS>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  if (e != cudaSuccess) return e;
+  k<<<(unsigned)(BH * p.n_split), THREADS, SMEM, s>>>(m, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_decode_combine<E, HS><<<(unsigned)(BH * p.Tq), HS, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace deck
+
+int decode_chunk(bool f32) { return f32 ? deck::Chunk<float>::N : deck::Chunk<uint16_t>::N; }
+
+size_t decode_workspace_bytes(int B, int L, int C, int NH, int Tq, bool f32) {
+  const int hs = C / NH;
+  const size_t n_split = (size_t)(L + decode_chunk(f32) - 1) / decode_chunk(f32);
+  return (size_t)B * NH * n_split * Tq * (hs + 2) * 4;
+}
+
+int decode_max_tq() { return deck::MAX_TQ; }
+
+// map_qkv: qkv as {3C, L, B}, box {hs, chunk rows, 1}, no swizzle
+cudaError_t launch_decode(const CUtensorMap& map_qkv, const void* qkv, void* out, float* lse, float* part, bool f32,
+                          int B, int L, int C, int NH, int Tq, cudaStream_t stream) {
+  deck::Params p;
+  p.qkv = qkv;
+  p.out = out;
+  p.lse = lse;
+  p.part = part;
+  p.err = device_error_word();
+  p.L = L;
+  p.C = C;
+  p.NH = NH;
+  p.Tq = Tq;
+  p.n_split = (L + decode_chunk(f32) - 1) / decode_chunk(f32);
+  const int hs = C / NH;
+  p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)hs));
+  const int BH = B * NH;
+  if (f32)
+    return hs == 64 ? deck::launch_t<float, 64>(map_qkv, p, BH, stream) : deck::launch_t<float, 32>(map_qkv, p, BH, stream);
+  return hs == 64 ? deck::launch_t<uint16_t, 64>(map_qkv, p, BH, stream)
+                  : deck::launch_t<uint16_t, 32>(map_qkv, p, BH, stream);
+}
+
+}  // namespace attn

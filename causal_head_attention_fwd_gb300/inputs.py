@@ -100,6 +100,33 @@ WORKLOADS = {
 }
 
 
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """A decode step: the last Tq tokens of L-token sequences attend to their cache."""
+    name: str
+    B: int
+    L: int
+    C: int
+    NH: int
+    Tq: int
+    dtype: str
+    sigma_qkv: float
+    seed_qkv: int
+
+    @property
+    def hs(self) -> int:
+        return self.C // self.NH
+
+
+# Decode stand-ins (the pages name the inference step offset but no decode
+# shape): a batch of 64 GPT-2-small sequences with a 4096-token cache, one new
+# token each, and the same with four new tokens (a short draft to verify).
+DECODE_WORKLOADS = {
+    "gpt2s_decode": DecodeWorkload("gpt2s_decode", 64, 4096, 768, 12, 1, "bf16", 0.5, 3000),
+    "gpt2s_decode4": DecodeWorkload("gpt2s_decode4", 64, 4096, 768, 12, 4, "bf16", 0.5, 3001),
+}
+
+
 @dataclasses.dataclass
 class HostInputs:
     """Host arrays for one workload.

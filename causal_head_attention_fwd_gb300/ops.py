@@ -67,6 +67,22 @@ def attention_matrices(qkv: torch.Tensor, lse: torch.Tensor, n_head: int, causal
     return pa, at
 
 
+def attention_decode(qkv: torch.Tensor, n_head: int, n_new: int, out=None, lse=None, workspace=None,
+                     stream=None):
+    """Decode forward: the last n_new rows of qkv (B, L, 3C) attend to every
+    key up to their own position. Returns out (B, n_new, C), lse (B, NH, n_new)."""
+    B, L, C, NH = _shape(qkv, n_head)
+    if out is None:
+        out = torch.empty((B, n_new, C), dtype=qkv.dtype, device=qkv.device)
+    if lse is None:
+        lse = torch.empty((B, NH, n_new), dtype=torch.float32, device=qkv.device)
+    dt = _DT[qkv.dtype]
+    nbytes = api.attn_decode_workspace_size(B, L, C, NH, n_new, dt)
+    ws = (workspace or _decode_ws).get(nbytes, qkv.device)
+    api.attn_decode(qkv, out, lse, B, L, C, NH, n_new, dt, ws, nbytes, stream)
+    return out, lse
+
+
 class Workspace:
     """Reusable device scratch buffer for attn_bwd (grown on demand)."""
 
@@ -82,6 +98,7 @@ class Workspace:
 
 
 _default_ws = Workspace()
+_decode_ws = Workspace()
 
 
 def attention_backward(dout, qkv, out, lse, n_head: int, causal: bool = True, dqkv=None,

@@ -103,6 +103,23 @@ attn_status_t attn_bwd(const void* dout, const void* qkv, const void* out, const
 attn_status_t attn_fwd_att(const void* qkv, const float* lse, float* preatt, float* att, int B, int T, int C,
                            int NH, int causal, attn_dtype_t dtype, void* stream);
 
+/*
+ * Decode forward (inference): the newest Tq tokens of each sequence attend to
+ * the key/value cache up to their own position (the pages' autoregressive
+ * `step` offset). llm.c's layout: qkv (B, L, 3C) holds K and V of positions
+ * 0..L-1 (the cache, new tokens included) and, in its last Tq rows, the new
+ * queries; query i (position L-Tq+i) sees keys 0..L-Tq+i.
+ *   out : (B, Tq, C) dtype, fully overwritten.
+ *   lse : (B, NH, Tq) fp32, natural-log logsumexp of the scaled scores.
+ *   workspace : attn_decode_workspace_size(...) bytes, 256-byte aligned,
+ *               owned by the caller (per-chunk partial results).
+ * 1 <= Tq <= min(L, 8); hs in {32, 64}. A stream over the cache, bound by HBM
+ * bandwidth; runs on the CUDA cores (fp32 arithmetic), not the tensor core.
+ */
+size_t attn_decode_workspace_size(int B, int L, int C, int NH, int Tq, attn_dtype_t dtype);
+attn_status_t attn_decode(const void* qkv, void* out, float* lse, int B, int L, int C, int NH, int Tq,
+                          attn_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* attn_status_string(attn_status_t status);
 
