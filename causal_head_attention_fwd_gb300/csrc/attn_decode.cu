@@ -1,8 +1,10 @@
 // Decode forward: a few new query tokens attending to a key/value cache.
 //
-// In autoregressive inference (the pages' inference setting, where a `step`
-// offset places the new tokens after the ones already processed) the newest
-// Tq tokens of each sequence attend to every key up to their own position.
+// In autoregressive inference ("LLM Systems 10 & 11: Accelerating Transformer
+// Training and Inference", §2.2, and the `step` offset of its §1 fused
+// embedding kernel, which places the new tokens after the ones already
+// processed) the newest Tq tokens of each sequence attend to every key up to
+// their own position.
 // The layout stays llm.c's: qkv is (B, L, 3C); its K and V slots for positions
 // 0..L-1 are the cache (the new tokens included), and the queries are the last
 // Tq rows. Query i sits at position p_i = L - Tq + i and sees keys 0..p_i:

@@ -105,8 +105,12 @@ attn_status_t attn_fwd_att(const void* qkv, const float* lse, float* preatt, flo
 
 /*
  * Decode forward (inference): the newest Tq tokens of each sequence attend to
- * the key/value cache up to their own position (the pages' autoregressive
- * `step` offset). llm.c's layout: qkv (B, L, 3C) holds K and V of positions
+ * the key/value cache up to their own position. Defined by "LLM Systems 10 &
+ * 11: Accelerating Transformer Training and Inference": §1, the fused
+ * embedding kernel's `step` argument (the autoregressive decoding offset, 0 in
+ * training), and §2.2, GPU inference (no intermediates or gradients kept), on
+ * the causal attention of llm.c `dev/cuda/attention_backward.cu`
+ * (attention_forward_cpu). llm.c's layout: qkv (B, L, 3C) holds K and V of positions
  * 0..L-1 (the cache, new tokens included) and, in its last Tq rows, the new
  * queries; query i (position L-Tq+i) sees keys 0..L-Tq+i.
  *   out : (B, Tq, C) dtype, fully overwritten.
