@@ -262,6 +262,63 @@ def run_att(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- FP8 forward
+FP8_PER_BF16 = 4.5 / 2.25     # nominal dense e4m3 / bf16 tensor rate of the GB300
+
+
+def run_fp8(args):
+    """Times attn_fwd_fp8 (e4m3 qkv with per-tensor descales, bf16 out) on one
+    GPU; FLOPs of the forward against the e4m3 tensor peak."""
+    import torch
+    from causal_head_attention_fwd_gb300 import build, inputs
+    build.build()
+    from causal_head_attention_fwd_gb300 import api, ops
+    dev = torch.device("cuda", 0)
+    w = inputs.FP8_WORKLOADS[args.fp8]
+    B, T, C, NH, causal = w["B"], w["T"], w["C"], w["NH"], w["causal"]
+    f = inputs.make_fp8_inputs(B, T, C, sigma=w["sigma"], seed=w["seed"])
+    codes = torch.from_numpy(f.codes).to(dev)
+    descale = torch.from_numpy(f.descale).to(dev)
+    out = torch.empty((B, T, C), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, NH, T), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        api.attn_fwd_fp8(codes, descale, out, lse, B, T, C, NH, int(causal), stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(0) as cs:
+        for a, b in ev:
+            flush.fill_(1.0)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+    if api.attn_last_device_error(stream) != api.ATTN_OK:
+        raise RuntimeError("device error in the timed region")
+    t_ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    fl = flops(B, T, C, NH, causal)["fwd"]
+    tf = fl / (t_ms * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    peak = float(peaks["bf16_tflops"]) * FP8_PER_BF16
+    line = {"metric": "FP8 (e4m3) attention forward TFLOP/s at 1 GB300", "value": tf, "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic",
+            "config": {"workload": f"{args.fp8}: B={B} T={T} C={C} NH={NH} causal={int(causal)}, e4m3 qkv, bf16 out",
+                       "B": B, "T": T, "C": C, "NH": NH, "l2": "flushed between timed steps (512 MiB write)"},
+            "roofline": {"kernel": "attn_fwd_fp8_kernel", "bound": "tensor", "achieved": tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,
+                         "peak_source": f"e4m3 = {src} bf16 burst (MEASURED_PEAKS.json bf16_tflops) x nominal 4.5/2.25"},
+            "gpu_launches": args.steps, "clocks": cs.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- decode forward
 def run_decode(args):
     """Times attn_decode (the last Tq tokens of each sequence against its whole
@@ -333,6 +390,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--decode", default=None, metavar="NAME",
                     help="time the decode forward (attn_decode) on a decode workload, e.g. gpt2s_decode")
+    ap.add_argument("--fp8", default=None, metavar="NAME",
+                    help="time the FP8 forward (attn_fwd_fp8) on an FP8 workload, e.g. gpt2s_fp8")
     ap.add_argument("--att", action="store_true",
                     help="time the llm.c drop-in mode (attn_fwd_att: preatt and att, B x NH x T x T fp32) "
                          "instead of the fwd+bwd step")
@@ -345,6 +404,8 @@ def main(argv=None):
         return run_att(args)
     if args.decode:
         return run_decode(args)
+    if args.fp8:
+        return run_fp8(args)
 
     import numpy as np
     import torch

@@ -28,7 +28,7 @@ ATTN_BF16 = 1
 EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_status_string",
             "attn_last_device_error", "attn_profile_enable", "attn_profile_reset",
             "attn_profile_read", "attn_bwd_noalloc", "attn_selftest_wait_timeout", "attn_fwd_att",
-            "attn_decode_workspace_size", "attn_decode")
+            "attn_decode_workspace_size", "attn_decode", "attn_fwd_fp8")
 
 # size of the fixed scratch array attn_bwd_noalloc uses (ATTN_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -81,6 +81,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_decode_workspace_size.restype = sz
     lib.attn_decode.argtypes = [vp, vp, f_p, i, i, i, i, i, i, vp, sz, vp]
     lib.attn_decode.restype = i
+    lib.attn_fwd_fp8.argtypes = [vp, f_p, vp, f_p, i, i, i, i, i, vp]
+    lib.attn_fwd_fp8.restype = i
     return lib
 
 
@@ -167,6 +169,15 @@ def attn_decode(qkv, out, lse, B, L, C, NH, Tq, dtype, workspace, workspace_byte
                           int(workspace_bytes), _stream(stream))
     if check and st != ATTN_OK:
         raise AttnError(st, "attn_decode")
+    return st
+
+
+def attn_fwd_fp8(qkv, descale, out, lse, B, T, C, NH, causal, stream=None, check=True) -> int:
+    """e4m3 qkv codes with per-tensor descales (device, 3 fp32) -> bf16 out, fp32 lse."""
+    st = _lib.attn_fwd_fp8(_ptr(qkv), _ptr(descale), _ptr(out), _ptr(lse), B, T, C, NH, int(causal),
+                           _stream(stream))
+    if check and st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_fp8")
     return st
 
 

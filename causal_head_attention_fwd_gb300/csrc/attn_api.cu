@@ -29,6 +29,8 @@ cudaError_t launch_bwd_f32(const CUtensorMap& map_q_l, const CUtensorMap& map_q_
                            const float* out, const float* lse, float* ws_D, const Problem& pr,
                            cudaStream_t stream);
 
+cudaError_t launch_fwd_fp8(const CUtensorMap& map_qkv, const CUtensorMap& map_out, const float* descale, float* lse,
+                           const Problem& pr, cudaStream_t stream);
 cudaError_t launch_att(const CUtensorMap& map_qkv, const float* lse, float* preatt, float* att, bool f32,
                        const Problem& pr, cudaStream_t stream);
 
@@ -224,6 +226,30 @@ extern "C" attn_status_t attn_fwd(const void* qkv, void* out, float* lse, int B,
       !encode_3d(&mo, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, T, B, pr.hs, BM, swz))
     return ATTN_ERR_CUDA;
   cudaError_t ce = launch_fwd_bf16(mq, mo, lse, pr, static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" attn_status_t attn_fwd_fp8(const void* qkv, const float* descale, void* out, float* lse, int B, int T,
+                                      int C, int NH, int causal, void* stream) {
+  attn_status_t st = check_shape(B, T, C, NH, causal, ATTN_BF16);
+  if (st != ATTN_OK) return st;
+  if (!qkv || !descale || !out || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(out) || !aligned16(lse) || (reinterpret_cast<uintptr_t>(descale) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  const size_t nq = (size_t)B * T * 3 * C, no = (size_t)B * T * C * 2, nl = (size_t)B * NH * T * 4, nd = 3 * 4;
+  if (overlaps(out, no, qkv, nq) || overlaps(lse, nl, qkv, nq) || overlaps(lse, nl, out, no) ||
+      overlaps(descale, nd, out, no) || overlaps(descale, nd, lse, nl))
+    return ATTN_ERR_INVALID_ARG;
+  Problem pr{B, T, C, NH, C / NH, causal};
+  if (!device_error_word() || device_sm_count() <= 0) return ATTN_ERR_CUDA;
+  // e4m3 tiles: hs-byte rows (64- or 32-byte swizzle); bf16 output as in attn_fwd
+  const CUtensorMapSwizzle s8 = pr.hs == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  const CUtensorMapSwizzle s16 = pr.hs == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUtensorMap mq, mo;
+  if (!encode_3d(&mq, qkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 3 * C, T, B, pr.hs, BM, s8) ||
+      !encode_3d(&mo, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, T, B, pr.hs, BM, s16))
+    return ATTN_ERR_CUDA;
+  cudaError_t ce = launch_fwd_fp8(mq, mo, descale, lse, pr, static_cast<cudaStream_t>(stream));
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

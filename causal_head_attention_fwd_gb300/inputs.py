@@ -153,6 +153,72 @@ def draw(shape, sigma: float, seed: int, dtype: str):
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
+# ----------------------------------------------------------------------------- e4m3
+# OCP FP8 E4M3 (the "fn" variant the tensor core reads): 1 sign bit, 4 exponent
+# bits (bias 7), 3 mantissa bits; exponent 0 holds the subnormals m * 2^-9;
+# no infinities; 0x7F / 0xFF are NaN, so the largest finite value is 448 (0x7E).
+
+E4M3_MAX = 448.0
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """float -> e4m3 codes (uint8): round to nearest, ties to even, saturating at +-448."""
+    x = np.asarray(x, dtype=np.float64)
+    sign = np.where(np.signbit(x), 0x80, 0x00).astype(np.uint8)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    code = np.zeros(a.shape, dtype=np.int64)
+    sub = a < 2.0 ** -6
+    # subnormal range (a rounding up to 8 * 2^-9 lands on the first normal code, 0x08)
+    code[sub] = np.rint(a[sub] * 2.0 ** 9).astype(np.int64)
+    an = a[~sub]
+    e = np.floor(np.log2(an)).astype(np.int64)
+    m = np.rint((an / np.exp2(e) - 1.0) * 8.0).astype(np.int64)     # 0..8
+    e = np.where(m == 8, e + 1, e)
+    m = np.where(m == 8, 0, m)
+    code[~sub] = np.minimum((e + 7) * 8 + m, 0x7E)
+    return (code.astype(np.uint8) | sign)
+
+
+def e4m3_decode(code: np.ndarray) -> np.ndarray:
+    """e4m3 codes (uint8) -> float64 values (NaN codes are not produced here)."""
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7))
+    return np.where(c & 0x80, -mag, mag)
+
+
+@dataclasses.dataclass
+class Fp8Inputs:
+    """qkv as e4m3 codes with one descale per q, k, v (value = code * descale)."""
+    codes: np.ndarray        # (B, T, 3C) uint8
+    descale: np.ndarray      # (3,) float32
+    qkv: np.ndarray          # (B, T, 3C) float64, the exact values the codes stand for
+
+
+def make_fp8_inputs(B, T, C, sigma=0.5, seed=1) -> Fp8Inputs:
+    """Draw qkv ~ N(0, sigma^2) (the bf16 recipe's normals), pick each tensor's
+    descale so its largest magnitude maps to the largest e4m3 code, quantise."""
+    x = normal_f64(seed, B * T * 3 * C).reshape(B, T, 3 * C) * sigma
+    codes = np.empty(x.shape, dtype=np.uint8)
+    descale = np.empty(3, dtype=np.float32)
+    for i in range(3):
+        part = x[:, :, i * C:(i + 1) * C]
+        d = np.float32(max(float(np.max(np.abs(part))), 1e-30) / E4M3_MAX)
+        descale[i] = d
+        codes[:, :, i * C:(i + 1) * C] = e4m3_encode(part / float(d))
+    vals = e4m3_decode(codes)
+    for i in range(3):
+        vals[:, :, i * C:(i + 1) * C] *= float(descale[i])
+    return Fp8Inputs(codes, descale, vals)
+
+
+# FP8 forward workload: the GPT-2-small training shape of the bf16 headline.
+FP8_WORKLOADS = {
+    "gpt2s_fp8": dict(B=16, T=1024, C=768, NH=12, causal=True, sigma=0.5, seed=4000),
+}
+
+
 def make_inputs(B, T, C, NH, dtype="bf16", sigma_qkv=0.5, sigma_dout=1e-2,
                 seed_qkv=1, seed_dout=2) -> HostInputs:
     del NH  # the layout does not depend on the head split

@@ -53,6 +53,21 @@ def attention_forward(qkv: torch.Tensor, n_head: int, causal: bool = True, out=N
     return out, lse
 
 
+def attention_forward_fp8(qkv_e4m3: torch.Tensor, descale: torch.Tensor, n_head: int, causal: bool = True,
+                          out=None, lse=None, stream=None):
+    """e4m3 qkv codes (uint8, (B, T, 3C)) and per-tensor descales (3 fp32 on the
+    device) -> out (B, T, C) bf16 and lse (B, NH, T) fp32."""
+    B, T, C, NH = _shape(qkv_e4m3, n_head)
+    if qkv_e4m3.dtype != torch.uint8 or descale.dtype != torch.float32 or descale.numel() != 3:
+        raise ValueError("qkv must be uint8 e4m3 codes and descale 3 float32 values")
+    if out is None:
+        out = torch.empty((B, T, C), dtype=torch.bfloat16, device=qkv_e4m3.device)
+    if lse is None:
+        lse = torch.empty((B, NH, T), dtype=torch.float32, device=qkv_e4m3.device)
+    api.attn_fwd_fp8(qkv_e4m3, descale, out, lse, B, T, C, NH, int(causal), stream)
+    return out, lse
+
+
 def attention_matrices(qkv: torch.Tensor, lse: torch.Tensor, n_head: int, causal: bool = True,
                        preatt=True, att=True, stream=None):
     """llm.c drop-in mode: (preatt, att), each (B, NH, T, T) fp32 or None.

@@ -62,6 +62,24 @@ attn_status_t attn_fwd(const void* qkv, void* out, float* lse, int B, int T, int
                        int causal, attn_dtype_t dtype, void* stream);
 
 /*
+ * FP8 forward: the forward in e4m3, the lower precision "LLM Systems 10 & 11:
+ * Accelerating Transformer Training and Inference" §1.3 (mixed-precision
+ * calculation) names for the forward next to FP16.
+ *   qkv     : (B, T, 3C) e4m3 codes (one byte each), llm.c's layout, read only.
+ *   descale : device array of 3 fp32, read only: the real value of a code of
+ *             q, k, v is code * descale[0], [1], [2] (one scale per tensor).
+ *   out     : (B, T, C) bf16, fully overwritten.
+ *   lse     : (B, NH, T) fp32, fully overwritten (natural log, scaled scores).
+ * q.k and P.V run on the tensor core in e4m3 with fp32 accumulation; the
+ * softmax probabilities enter P.V as e4m3 codes (relative rounding error at
+ * most 2^-4), the row sums and lse are formed from the fp32 probabilities.
+ * hs in {32, 64}; qkv, out, lse 16-byte aligned, descale 4-byte aligned; no
+ * buffer may overlap another (ATTN_ERR_INVALID_ARG).
+ */
+attn_status_t attn_fwd_fp8(const void* qkv, const float* descale, void* out, float* lse, int B, int T, int C,
+                           int NH, int causal, void* stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for this problem (0 if none).
  * Returns 0 also for arguments attn_bwd would reject.
  */
