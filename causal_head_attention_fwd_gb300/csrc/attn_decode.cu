@@ -76,7 +76,10 @@ struct Chunk {
   static constexpr int N = 128;
 };
 
-template <typename E, int HS>
+// TQ: the largest Tq this instantiation serves (1, 4 or 8); its per-query
+// shared arrays and accumulators are sized by it, so the common one-token step
+// keeps more CTAs resident per SM.
+template <typename E, int HS, int TQ>
 __global__ void __launch_bounds__(THREADS)
 attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
   // A K or V row (HS elements) is read by LPR lanes, 8 elements each, so a
@@ -88,11 +91,11 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   E* sK = reinterpret_cast<E*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   E* sV = sK + CH * HS;
-  __shared__ __align__(16) float sq[MAX_TQ][HS];
-  __shared__ float sp[MAX_TQ][CH];
-  __shared__ float red[MAX_TQ][THREADS / 32];
-  __shared__ float row_m[MAX_TQ];
-  __shared__ float sacc[THREADS / 32][MAX_TQ][HS];
+  __shared__ __align__(16) float sq[TQ][HS];
+  __shared__ float sp[TQ][CH];
+  __shared__ float red[TQ][THREADS / 32];
+  __shared__ float row_m[TQ];
+  __shared__ float sacc[THREADS / 32][TQ][HS];
   __shared__ uint64_t bar_k, bar_v;
   __shared__ volatile int abort_sh;
 
@@ -183,9 +186,9 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
   ok = mbar_wait(&bar_v, 0, &abort_sh, p.err) && ok;
   // partial outputs: each lane accumulates its 8 columns over its rows of the
   // chunk for every query, then the rows of a warp and the warps are summed
-  float acc[MAX_TQ][8];
+  float acc[TQ][8];
 #pragma unroll
-  for (int i = 0; i < MAX_TQ; ++i)
+  for (int i = 0; i < TQ; ++i)
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc[i][k] = 0.f;
 #pragma unroll 4
@@ -194,7 +197,7 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
     float vv[8];
     load8<E>(sV + j * HS + db, vv);               // rows past L are zero, their p is 0
 #pragma unroll
-    for (int i = 0; i < MAX_TQ; ++i) {
+    for (int i = 0; i < TQ; ++i) {
       if (i < Tq) {
         const float pj = sp[i][j];
 #pragma unroll
@@ -203,7 +206,7 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
     }
   }
 #pragma unroll
-  for (int i = 0; i < MAX_TQ; ++i) {
+  for (int i = 0; i < TQ; ++i) {
     if (i < Tq) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -268,7 +271,8 @@ __global__ void __launch_bounds__(HS) attn_decode_combine(const Params p) {
 template <typename E, int HS>
 static cudaError_t launch_t(const CUtensorMap& m, const Params& p, int BH, cudaStream_t s) {
   constexpr int SMEM = 2 * Chunk<E>::N * HS * (int)sizeof(E) + 128;
-  auto k = attn_decode_split<E, HS>;
+  auto k = p.Tq == 1 ? attn_decode_split<E, HS, 1>
+                     : (p.Tq <= 4 ? attn_decode_split<E, HS, 4> : attn_decode_split<E, HS, MAX_TQ>);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
   k<<<(unsigned)(BH * p.n_split), THREADS, SMEM, s>>>(m, p);
