@@ -108,6 +108,7 @@ template <int HS>
 __global__ void attn_bwd_pre(const uint4* __restrict__ dout, const uint4* __restrict__ out,
                              float* __restrict__ D, float4* __restrict__ dq_acc, int T, int C, int NH,
                              long long n_vec) {
+  pdl_launch_and_wait();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   constexpr int LANES = HS / 8;   // threads per head row
   float acc = 0.f;
@@ -142,6 +143,7 @@ __global__ void attn_bwd_pre(const uint4* __restrict__ dout, const uint4* __rest
 // ----------------------------------------------------------------------------
 __global__ void attn_bwd_dq_out(const float4* __restrict__ dq_acc, uint4* __restrict__ dqkv, int C,
                                 long long n_vec) {
+  pdl_launch_and_wait();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // 8 channels each
   if (i >= n_vec) return;
   const long long e = i * 8;
@@ -254,6 +256,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   int* gerr = p.err;
+  pdl_launch_and_wait();
 
   if (warp >= 8) {
     setmaxnreg_dec<REG_OTHER>();
@@ -574,8 +577,7 @@ static cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& md,
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<HS>::ALLOC);
   if (e != cudaSuccess) return e;
   ProfileScope ps(K_BWD_MAIN, stream);
-  k<<<grid, BWD_THREADS, BwdSmem<HS>::ALLOC, stream>>>(mq, md, mg, macc, p);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(grid), dim3(BWD_THREADS), BwdSmem<HS>::ALLOC, stream, mq, md, mg, macc, p);
 }
 
 cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_dout,
@@ -588,15 +590,9 @@ cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_d
   cudaError_t e;
   {
     ProfileScope ps(K_BWD_PRE, stream);
-    if (pr.hs == 64)
-      attn_bwd_pre<64><<<(unsigned)blocks, threads, 0, stream>>>(
-          static_cast<const uint4*>(dout), static_cast<const uint4*>(out), ws_D,
-          reinterpret_cast<float4*>(ws_dq), pr.T, pr.C, pr.NH, n_vec);
-    else
-      attn_bwd_pre<32><<<(unsigned)blocks, threads, 0, stream>>>(
-          static_cast<const uint4*>(dout), static_cast<const uint4*>(out), ws_D,
-          reinterpret_cast<float4*>(ws_dq), pr.T, pr.C, pr.NH, n_vec);
-    e = cudaGetLastError();
+    e = launch_pdl(pr.hs == 64 ? attn_bwd_pre<64> : attn_bwd_pre<32>, dim3((unsigned)blocks), dim3(threads), 0,
+                   stream, static_cast<const uint4*>(dout), static_cast<const uint4*>(out), ws_D,
+                   reinterpret_cast<float4*>(ws_dq), pr.T, pr.C, pr.NH, n_vec);
   }
   if (e != cudaSuccess) return e;
 
@@ -623,9 +619,8 @@ cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_d
   if (e != cudaSuccess) return e;
 
   ProfileScope ps(K_BWD_DQ, stream);
-  attn_bwd_dq_out<<<(unsigned)blocks, threads, 0, stream>>>(reinterpret_cast<const float4*>(ws_dq),
-                                                            static_cast<uint4*>(dqkv), pr.C, n_vec);
-  return cudaGetLastError();
+  return launch_pdl(attn_bwd_dq_out, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                    reinterpret_cast<const float4*>(ws_dq), static_cast<uint4*>(dqkv), pr.C, n_vec);
 }
 
 }  // namespace attn

@@ -141,6 +141,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   int* gerr = p.err;
+  pdl_launch_and_wait();
 
   if (warp >= 8) {
   setmaxnreg_dec<FREG_OTHER>();
@@ -412,8 +413,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mo, co
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdSmem<HS>::ALLOC);
   if (e != cudaSuccess) return e;
   ProfileScope ps(K_FWD, stream);
-  k<<<grid, FWD_THREADS, FwdSmem<HS>::ALLOC, stream>>>(mq, mo, p);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(grid), dim3(FWD_THREADS), FwdSmem<HS>::ALLOC, stream, mq, mo, p);
 }
 
 cudaError_t launch_fwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_out, float* lse,

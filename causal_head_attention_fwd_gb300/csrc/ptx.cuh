@@ -339,6 +339,17 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                :: "l"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
+// Programmatic dependent launch. Let the next kernel on the stream begin
+// launching (it gets SMs only as this kernel's CTAs leave them), then wait
+// until every kernel this one depends on has completed and its memory is
+// visible. Called before the kernel touches global memory, so no read or
+// write can overlap a neighbouring kernel's. Without the launch attribute
+// both instructions are no-ops.
+__device__ __forceinline__ void pdl_launch_and_wait() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // --------------------------------------------------------------------------
 // numeric helpers
 // --------------------------------------------------------------------------
