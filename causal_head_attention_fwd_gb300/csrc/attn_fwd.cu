@@ -30,7 +30,7 @@
 
 namespace attn {
 
-constexpr int FWD_STAGES = 3;
+constexpr int FWD_STAGES = 4;
 constexpr int FWD_THREADS = 384;
 // register split: the two softmax warpgroups up, the producer/MMA warpgroup down
 constexpr uint32_t FREG_SOFTMAX = 208, FREG_OTHER = 80;
