@@ -319,6 +319,78 @@ def run_fp8(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- attention block
+def run_block(args):
+    """Times the GPT-2 attention block forward: c_attn GEMM (+bias) -> attention
+    forward -> c_proj GEMM (+bias), three launches on one stream."""
+    import torch
+    from causal_head_attention_fwd_gb300 import build, inputs
+    build.build()
+    from causal_head_attention_fwd_gb300 import api, ops
+    dev = torch.device("cuda", 0)
+    w = inputs.BLOCK_WORKLOADS[args.block]
+    B, T, C, NH, causal = w["B"], w["T"], w["C"], w["NH"], w["causal"]
+    bi = inputs.make_block_inputs(B, T, C, seed=w["seed"])
+    d = {k: ops.upload(v, "bf16", dev) for k, v in bi.bits.items()}
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    qkv = torch.empty((B, T, 3 * C), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((B, T, C), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, NH, T), dtype=torch.float32, device=dev)
+    y = torch.empty((B, T, C), dtype=torch.bfloat16, device=dev)
+    M = B * T
+
+    def step():
+        api.attn_linear_fwd(d["x"], d["w_attn"], d["b_attn"], qkv, M, 3 * C, C, stream)
+        api.attn_fwd(qkv, out, lse, B, T, C, NH, int(causal), api.ATTN_BF16, stream)
+        api.attn_linear_fwd(out, d["w_proj"], d["b_proj"], y, M, C, C, stream)
+
+    def timed(n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in ev:
+            flush.fill_(1.0)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in ev]
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(0) as cs:
+        times = timed(args.steps)
+    if api.attn_last_device_error(stream) != api.ATTN_OK:
+        raise RuntimeError("device error in the timed region")
+    t_ms = sum(times) / len(times)
+    f_lin = 2.0 * M * 3 * C * C + 2.0 * M * C * C
+    f_att = flops(B, T, C, NH, causal)["fwd"]
+    tf = (f_lin + f_att) / (t_ms * 1e-3) / 1e12
+    api.attn_profile_reset()
+    api.attn_profile_enable(True)
+    timed(20)
+    api.attn_profile_enable(False)
+    lin_ms, lin_n = api.attn_profile_read(api.K_LINEAR)
+    att_ms, att_n = api.attn_profile_read(api.K_FWD)
+    peaks, src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    lin_tf = f_lin / (lin_ms / max(lin_n, 1) * 2 * 1e-3) / 1e12
+    line = {"metric": "GPT-2 attention block forward (c_attn + attention + c_proj) TFLOP/s at 1 GB300",
+            "value": tf, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"{args.block}: B={B} T={T} C={C} NH={NH} causal={int(causal)}, bf16",
+                       "B": B, "T": T, "C": C, "NH": NH, "l2": "flushed between timed steps (512 MiB write)"},
+            "kernels": {"attn_linear_kernel": {"launches": lin_n, "avg_ms": lin_ms / max(lin_n, 1)},
+                        "attn_fwd_kernel": {"launches": att_n, "avg_ms": att_ms / max(att_n, 1)}},
+            "roofline": {"kernel": "attn_linear_kernel (c_attn + c_proj)", "bound": "tensor", "achieved": lin_tf,
+                         "peak": peak, "unit": "TFLOP/s", "frac": lin_tf / peak, "traffic": None,
+                         "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)"},
+            "gpu_launches": 3 * args.steps, "clocks": cs.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- decode forward
 def run_decode(args):
     """Times attn_decode (the last Tq tokens of each sequence against its whole
@@ -392,6 +464,8 @@ def main(argv=None):
                     help="time the decode forward (attn_decode) on a decode workload, e.g. gpt2s_decode")
     ap.add_argument("--fp8", default=None, metavar="NAME",
                     help="time the FP8 forward (attn_fwd_fp8) on an FP8 workload, e.g. gpt2s_fp8")
+    ap.add_argument("--block", default=None, metavar="NAME",
+                    help="time the GPT-2 attention block forward (c_attn -> attention -> c_proj), e.g. gpt2s_block")
     ap.add_argument("--att", action="store_true",
                     help="time the llm.c drop-in mode (attn_fwd_att: preatt and att, B x NH x T x T fp32) "
                          "instead of the fwd+bwd step")
@@ -406,6 +480,8 @@ def main(argv=None):
         return run_decode(args)
     if args.fp8:
         return run_fp8(args)
+    if args.block:
+        return run_block(args)
 
     import numpy as np
     import torch

@@ -28,13 +28,13 @@ ATTN_BF16 = 1
 EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_status_string",
             "attn_last_device_error", "attn_profile_enable", "attn_profile_reset",
             "attn_profile_read", "attn_bwd_noalloc", "attn_selftest_wait_timeout", "attn_fwd_att",
-            "attn_decode_workspace_size", "attn_decode", "attn_fwd_fp8")
+            "attn_decode_workspace_size", "attn_decode", "attn_fwd_fp8", "attn_linear_fwd")
 
 # size of the fixed scratch array attn_bwd_noalloc uses (ATTN_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # kernel ids of attn_profile_read
-K_FWD, K_BWD_PRE, K_BWD_MAIN, K_BWD_DQ = 0, 1, 2, 3
+K_FWD, K_BWD_PRE, K_BWD_MAIN, K_BWD_DQ, K_LINEAR = 0, 1, 2, 3, 4
 KERNEL_NAMES = {K_FWD: "attn_fwd_kernel", K_BWD_PRE: "attn_bwd_pre",
                 K_BWD_MAIN: "attn_bwd_kernel", K_BWD_DQ: "attn_bwd_dq_out"}
 # The same four profiling slots hold the fp32 path's kernels.
@@ -83,6 +83,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_decode.restype = i
     lib.attn_fwd_fp8.argtypes = [vp, f_p, vp, f_p, i, i, i, i, i, vp]
     lib.attn_fwd_fp8.restype = i
+    lib.attn_linear_fwd.argtypes = [vp, vp, vp, vp, i, i, i, vp]
+    lib.attn_linear_fwd.restype = i
     return lib
 
 
@@ -178,6 +180,14 @@ def attn_fwd_fp8(qkv, descale, out, lse, B, T, C, NH, causal, stream=None, check
                            _stream(stream))
     if check and st != ATTN_OK:
         raise AttnError(st, "attn_fwd_fp8")
+    return st
+
+
+def attn_linear_fwd(inp, weight, bias, out, M, N, K, stream=None, check=True) -> int:
+    """out (M, N) = inp (M, K) . weight (N, K)^T + bias (N), bf16; bias may be None."""
+    st = _lib.attn_linear_fwd(_ptr(inp), _ptr(weight), _ptr(bias), _ptr(out), M, N, K, _stream(stream))
+    if check and st != ATTN_OK:
+        raise AttnError(st, "attn_linear_fwd")
     return st
 
 

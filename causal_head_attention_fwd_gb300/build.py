@@ -24,7 +24,7 @@ BUILD = ROOT / "_build"
 LIB = PKG / "libattn.so"
 
 SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_f32.cu", "attn_bwd_noalloc.cu", "attn_selftest.cu", "attn_att.cu", "attn_decode.cu",
-           "attn_fwd_fp8.cu"]
+           "attn_fwd_fp8.cu", "attn_linear.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "--expt-relaxed-constexpr", "-I", str(INCLUDE), "-I", str(CSRC)]

@@ -31,6 +31,8 @@ cudaError_t launch_bwd_f32(const CUtensorMap& map_q_l, const CUtensorMap& map_q_
 
 cudaError_t launch_fwd_fp8(const CUtensorMap& map_qkv, const CUtensorMap& map_out, const float* descale, float* lse,
                            const Problem& pr, cudaStream_t stream);
+cudaError_t launch_linear(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
+                          const void* bias, int M, int N, int K, cudaStream_t stream);
 cudaError_t launch_att(const CUtensorMap& map_qkv, const float* lse, float* preatt, float* att, bool f32,
                        const Problem& pr, cudaStream_t stream);
 
@@ -78,9 +80,9 @@ struct ProfState {
   struct Pending { cudaEvent_t a, b; };
   std::vector<Pending> pending[K_COUNT];
   std::vector<cudaEvent_t> pool;
-  double total_ms[K_COUNT] = {0, 0, 0, 0};
-  long long count[K_COUNT] = {0, 0, 0, 0};
-  cudaEvent_t cur_begin[K_COUNT] = {nullptr, nullptr, nullptr, nullptr};
+  double total_ms[K_COUNT] = {};
+  long long count[K_COUNT] = {};
+  cudaEvent_t cur_begin[K_COUNT] = {};
 };
 static ProfState g_prof;
 
@@ -250,6 +252,28 @@ extern "C" attn_status_t attn_fwd_fp8(const void* qkv, const float* descale, voi
       !encode_3d(&mo, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, T, B, pr.hs, BM, s16))
     return ATTN_ERR_CUDA;
   cudaError_t ce = launch_fwd_fp8(mq, mo, descale, lse, pr, static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" attn_status_t attn_linear_fwd(const void* inp, const void* weight, const void* bias, void* out, int M,
+                                         int N, int K, void* stream) {
+  if (M < 1 || N < 1 || K < 1) return ATTN_ERR_INVALID_ARG;
+  if (N % 8 != 0 || K % 8 != 0) return ATTN_ERR_UNSUPPORTED;     // 16-byte row strides for the tensor copies
+  if ((double)((M + 127) / 128) * ((N + 255) / 256) > 2.0e9) return ATTN_ERR_INVALID_ARG;   // tile count fits an int
+  if (!inp || !weight || !out) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(inp) || !aligned16(weight) || !aligned16(out) || (bias && !aligned16(bias)))
+    return ATTN_ERR_MISALIGNED;
+  const size_t ni = (size_t)M * K * 2, nw = (size_t)N * K * 2, no = (size_t)M * N * 2, nb = (size_t)N * 2;
+  if (overlaps(out, no, inp, ni) || overlaps(out, no, weight, nw) || (bias && overlaps(out, no, bias, nb)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!device_error_word() || device_sm_count() <= 0) return ATTN_ERR_CUDA;
+  CUtensorMap ma, mb, mo;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle w = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (!encode_3d(&ma, inp, bf, 2, K, M, 1, 64, 128, w) || !encode_3d(&mb, weight, bf, 2, K, N, 1, 64, 256, w) ||
+      !encode_3d(&mo, out, bf, 2, N, M, 1, 64, 128, w))
+    return ATTN_ERR_CUDA;
+  cudaError_t ce = launch_linear(ma, mb, mo, bias, M, N, K, static_cast<cudaStream_t>(stream));
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

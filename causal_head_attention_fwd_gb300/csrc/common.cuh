@@ -45,7 +45,7 @@ int* device_error_word();
 int device_sm_count();
 
 // Optional per-kernel timing (see attn_profile_enable in include/attn.h).
-enum KernelId { K_FWD = 0, K_BWD_PRE = 1, K_BWD_MAIN = 2, K_BWD_DQ = 3, K_COUNT = 4 };
+enum KernelId { K_FWD = 0, K_BWD_PRE = 1, K_BWD_MAIN = 2, K_BWD_DQ = 3, K_LINEAR = 4, K_COUNT = 5 };
 void profile_begin(KernelId k, cudaStream_t s);
 void profile_end(KernelId k, cudaStream_t s);
 

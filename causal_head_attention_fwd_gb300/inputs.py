@@ -219,6 +219,34 @@ FP8_WORKLOADS = {
 }
 
 
+# ----------------------------------------------------------------------------- attention block
+@dataclasses.dataclass
+class BlockInputs:
+    """x and the c_attn / c_proj parameters, bf16: exact values (float32) and bits."""
+    x: np.ndarray
+    w_attn: np.ndarray
+    b_attn: np.ndarray
+    w_proj: np.ndarray
+    b_proj: np.ndarray
+    bits: dict
+
+
+def make_block_inputs(B, T, C, seed=5000, sigma_w=0.02) -> BlockInputs:
+    """GPT-2 scales: x ~ N(0, 1) (a layer-normed residual), weights and biases
+    ~ N(0, sigma_w^2) (GPT-2's initialisation scale), all rounded to bf16."""
+    vals, bits = {}, {}
+    for i, (name, shape, sig) in enumerate([("x", (B, T, C), 1.0), ("w_attn", (3 * C, C), sigma_w),
+                                            ("b_attn", (3 * C,), sigma_w), ("w_proj", (C, C), sigma_w),
+                                            ("b_proj", (C,), sigma_w)]):
+        vals[name], bits[name] = draw(shape, sig, seed + i, "bf16")
+    return BlockInputs(vals["x"], vals["w_attn"], vals["b_attn"], vals["w_proj"], vals["b_proj"], bits)
+
+
+BLOCK_WORKLOADS = {
+    "gpt2s_block": dict(B=16, T=1024, C=768, NH=12, causal=True, seed=5000),
+}
+
+
 def make_inputs(B, T, C, NH, dtype="bf16", sigma_qkv=0.5, sigma_dout=1e-2,
                 seed_qkv=1, seed_dout=2) -> HostInputs:
     del NH  # the layout does not depend on the head split

@@ -68,6 +68,31 @@ def attention_forward_fp8(qkv_e4m3: torch.Tensor, descale: torch.Tensor, n_head:
     return out, lse
 
 
+def linear(inp: torch.Tensor, weight: torch.Tensor, bias=None, out=None, stream=None):
+    """out (..., N) = inp (..., K) . weight (N, K)^T + bias (N), bf16 (fused bias epilogue)."""
+    if inp.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise ValueError("linear takes bf16 tensors")
+    if not (inp.is_contiguous() and weight.is_contiguous()):
+        raise ValueError("inp and weight must be contiguous")
+    K = inp.shape[-1]
+    N = weight.shape[0]
+    M = inp.numel() // K
+    if out is None:
+        out = torch.empty((*inp.shape[:-1], N), dtype=torch.bfloat16, device=inp.device)
+    api.attn_linear_fwd(inp, weight, bias, out, M, N, K, stream)
+    return out
+
+
+def attention_block_forward(x: torch.Tensor, w_attn, b_attn, w_proj, b_proj, n_head: int, causal: bool = True,
+                            stream=None):
+    """GPT-2 attention block forward: qkv = c_attn(x) -> attention -> y = c_proj(out).
+    Returns (y, qkv, out, lse); three launches on one stream."""
+    qkv = linear(x, w_attn, b_attn, stream=stream)
+    out, lse = attention_forward(qkv, n_head, causal, stream=stream)
+    y = linear(out, w_proj, b_proj, stream=stream)
+    return y, qkv, out, lse
+
+
 def attention_matrices(qkv: torch.Tensor, lse: torch.Tensor, n_head: int, causal: bool = True,
                        preatt=True, att=True, stream=None):
     """llm.c drop-in mode: (preatt, att), each (B, NH, T, T) fp32 or None.

@@ -80,6 +80,25 @@ attn_status_t attn_fwd_fp8(const void* qkv, const float* descale, void* out, flo
                            int NH, int causal, void* stream);
 
 /*
+ * Linear layer of the GPT-2 attention block (c_attn: x -> qkv, c_proj:
+ * attention out -> y), with the bias add fused into the GEMM epilogue
+ * ("LLM Systems 10 & 11: Accelerating Transformer Training and Inference"
+ * §1.1, kernel fusion of the non-GEMM ops of the MHA layer):
+ *   out[m, o] = bias[o] + sum_k inp[m, k] * weight[o, k]
+ *   inp    : (M, K) bf16, row-major, read only.
+ *   weight : (N, K) bf16, row-major (llm.c's (OC, C) layout), read only.
+ *   bias   : (N) bf16, read only, or NULL for none.
+ *   out    : (M, N) bf16, fully overwritten; must not overlap the inputs.
+ * tcgen05 tensor cores, fp32 accumulation, one bf16 rounding of the result.
+ * N % 8 == 0 and K % 8 == 0 (ATTN_ERR_UNSUPPORTED otherwise); pointers
+ * 16-byte aligned. A GPT-2 attention block forward is attn_linear_fwd
+ * (N = 3C) -> attn_fwd -> attn_linear_fwd (N = C) on one stream; the three
+ * launches overlap their start-up with the previous kernel's tail.
+ */
+attn_status_t attn_linear_fwd(const void* inp, const void* weight, const void* bias, void* out, int M, int N,
+                              int K, void* stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for this problem (0 if none).
  * Returns 0 also for arguments attn_bwd would reject.
  */
@@ -196,11 +215,11 @@ attn_status_t attn_selftest_wait_timeout(unsigned int limit_us, void* stream);
  * synchronises those events and returns the accumulated device time (ms) and
  * launch count of one kernel since the last reset. Kernel ids:
  *   0 forward, 1 backward pre-pass (D, zero dq accumulator),
- *   2 backward main kernel, 3 backward dq conversion.
+ *   2 backward main kernel, 3 backward dq conversion, 4 linear layer.
  * Enabling adds two event records per launch; leave it off for timing runs.
  * Not thread-safe with concurrent attn_fwd/attn_bwd calls from other threads.
  */
-#define ATTN_PROFILE_NUM_KERNELS 4
+#define ATTN_PROFILE_NUM_KERNELS 5
 attn_status_t attn_profile_enable(int enable);
 attn_status_t attn_profile_reset(void);
 attn_status_t attn_profile_read(int kernel_id, double* total_ms, long long* launches);

@@ -10,3 +10,4 @@ library cross-checks); see tests/test_oracle_pins.py.
 """
 from .attention import (forward, backward, head_forward, head_backward,  # noqa: F401
                         head_dpreatt_jacobian, split_heads, row_stat_D)
+from .layer import linear, block_forward  # noqa: F401
