@@ -28,7 +28,8 @@ ATTN_BF16 = 1
 EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_status_string",
             "attn_last_device_error", "attn_profile_enable", "attn_profile_reset",
             "attn_profile_read", "attn_bwd_noalloc", "attn_selftest_wait_timeout", "attn_fwd_att",
-            "attn_decode_workspace_size", "attn_decode", "attn_fwd_fp8", "attn_linear_fwd")
+            "attn_decode_workspace_size", "attn_decode", "attn_fwd_fp8", "attn_linear_fwd",
+            "attn_bwd_fp8_workspace_size", "attn_bwd_fp8")
 
 # size of the fixed scratch array attn_bwd_noalloc uses (ATTN_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -85,6 +86,10 @@ def _load() -> ctypes.CDLL:
     lib.attn_fwd_fp8.restype = i
     lib.attn_linear_fwd.argtypes = [vp, vp, vp, vp, i, i, i, vp]
     lib.attn_linear_fwd.restype = i
+    lib.attn_bwd_fp8_workspace_size.argtypes = [i, i, i, i, i]
+    lib.attn_bwd_fp8_workspace_size.restype = sz
+    lib.attn_bwd_fp8.argtypes = [vp, vp, f_p, vp, f_p, vp, i, i, i, i, i, vp, sz, vp]
+    lib.attn_bwd_fp8.restype = i
     return lib
 
 
@@ -180,6 +185,19 @@ def attn_fwd_fp8(qkv, descale, out, lse, B, T, C, NH, causal, stream=None, check
                            _stream(stream))
     if check and st != ATTN_OK:
         raise AttnError(st, "attn_fwd_fp8")
+    return st
+
+
+def attn_bwd_fp8_workspace_size(B, T, C, NH, causal) -> int:
+    return int(_lib.attn_bwd_fp8_workspace_size(B, T, C, NH, int(causal)))
+
+
+def attn_bwd_fp8(dout, qkv, descale, out, lse, dqkv, B, T, C, NH, causal, workspace, workspace_bytes,
+                 stream=None, check=True) -> int:
+    st = _lib.attn_bwd_fp8(_ptr(dout), _ptr(qkv), _ptr(descale), _ptr(out), _ptr(lse), _ptr(dqkv), B, T, C, NH,
+                           int(causal), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    if check and st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_fp8")
     return st
 
 

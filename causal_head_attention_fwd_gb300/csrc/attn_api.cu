@@ -31,6 +31,8 @@ cudaError_t launch_bwd_f32(const CUtensorMap& map_q_l, const CUtensorMap& map_q_
 
 cudaError_t launch_fwd_fp8(const CUtensorMap& map_qkv, const CUtensorMap& map_out, const float* descale, float* lse,
                            const Problem& pr, cudaStream_t stream);
+cudaError_t launch_fp8_dequant(const void* codes, const float* descale, void* out, int B, int T, int C,
+                               cudaStream_t stream);
 cudaError_t launch_linear(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
                           const void* bias, int M, int N, int K, cudaStream_t stream);
 cudaError_t launch_att(const CUtensorMap& map_qkv, const float* lse, float* preatt, float* att, bool f32,
@@ -275,6 +277,46 @@ extern "C" attn_status_t attn_linear_fwd(const void* inp, const void* weight, co
     return ATTN_ERR_CUDA;
   cudaError_t ce = launch_linear(ma, mb, mo, bias, M, N, K, static_cast<cudaStream_t>(stream));
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// FP8 backward scratch: the bf16 expansion of qkv (B*T*3C*2 bytes, 256-byte
+// aligned), then attn_bwd's own bf16 workspace.
+static size_t fp8_qkv_bytes(int B, int T, int C) { return (((size_t)B * T * 3 * C * 2) + 255) & ~(size_t)255; }
+
+extern "C" size_t attn_bwd_fp8_workspace_size(int B, int T, int C, int NH, int causal) {
+  if (check_shape(B, T, C, NH, causal, ATTN_BF16) != ATTN_OK) return 0;
+  return fp8_qkv_bytes(B, T, C) + attn_bwd_workspace_size(B, T, C, NH, causal, ATTN_BF16);
+}
+
+extern "C" attn_status_t attn_bwd_fp8(const void* dout, const void* qkv, const float* descale, const void* out,
+                                      const float* lse, void* dqkv, int B, int T, int C, int NH, int causal,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  attn_status_t st = check_shape(B, T, C, NH, causal, ATTN_BF16);
+  if (st != ATTN_OK) return st;
+  if (!dout || !qkv || !descale || !out || !lse || !dqkv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(dout) || !aligned16(qkv) || !aligned16(out) || !aligned16(lse) || !aligned16(dqkv) ||
+      (reinterpret_cast<uintptr_t>(descale) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  const size_t need = attn_bwd_fp8_workspace_size(B, T, C, NH, causal);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_MISALIGNED;
+  const size_t n8 = (size_t)B * T * 3 * C, n3 = n8 * 2, n1 = (size_t)B * T * C * 2, nl = (size_t)B * NH * T * 4;
+  if (overlaps(dqkv, n3, qkv, n8) || overlaps(dqkv, n3, out, n1) || overlaps(dqkv, n3, dout, n1) ||
+      overlaps(dqkv, n3, lse, nl) || overlaps(dqkv, n3, descale, 12) || overlaps(workspace, need, qkv, n8) ||
+      overlaps(workspace, need, out, n1) || overlaps(workspace, need, dout, n1) ||
+      overlaps(workspace, need, lse, nl) || overlaps(workspace, need, descale, 12) ||
+      overlaps(workspace, need, dqkv, n3))
+    return ATTN_ERR_INVALID_ARG;
+  if (!device_error_word() || device_sm_count() <= 0) return ATTN_ERR_CUDA;
+  // 1. the e4m3 codes expanded to bf16 values code * descale (the matmuls of the
+  //    backward run in bf16), 2. the bf16 backward on them
+  char* ws = static_cast<char*>(workspace);
+  void* qkv16 = ws;
+  if (launch_fp8_dequant(qkv, descale, qkv16, B, T, C, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const size_t off = fp8_qkv_bytes(B, T, C);
+  return attn_bwd(dout, qkv16, out, lse, dqkv, B, T, C, NH, causal, ATTN_BF16, ws + off, workspace_bytes - off,
+                  stream);
 }
 
 extern "C" size_t attn_bwd_workspace_size(int B, int T, int C, int NH, int causal, attn_dtype_t dtype) {

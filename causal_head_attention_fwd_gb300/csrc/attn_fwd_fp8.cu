@@ -466,3 +466,50 @@ cudaError_t launch_fwd_fp8(const CUtensorMap& map_qkv, const CUtensorMap& map_ou
 }
 
 }  // namespace attn
+
+namespace attn {
+namespace f8 {
+
+// e4m3 codes -> bf16 values code * descale[part] (part = q, k, v by column),
+// 16 codes per thread: one 16-byte load, two 16-byte stores.
+__global__ void attn_fp8_dequant(const uint4* __restrict__ codes, const float* __restrict__ descale,
+                                 uint4* __restrict__ out, int C, long long n16) {
+  pdl_launch_and_wait();
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n16) return;
+  const long long e = i * 16;                              // element index in (B, T, 3C)
+  const int col = (int)(e % (3LL * C));
+  const float d = __ldg(descale + col / C);                // C % 16 == 0: one part per thread
+  const uint4 v = codes[i];
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      // two e4m3 codes -> f16x2 (exact: e4m3 values are f16 values) -> f32 -> * descale -> bf16x2
+      const uint16_t pair = (uint16_t)(w[k] >> (16 * hlf));
+      uint32_t h2;
+      asm("{\n\t.reg .b16 c;\n\tmov.b16 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "h"(pair));
+      float lo, hi;
+      asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+          : "=f"(lo), "=f"(hi) : "r"(h2));
+      o[2 * k + hlf] = pack_bf16x2(lo * d, hi * d);
+    }
+  }
+  out[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+  out[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+}  // namespace f8
+
+cudaError_t launch_fp8_dequant(const void* codes, const float* descale, void* out, int B, int T, int C,
+                               cudaStream_t stream) {
+  const long long n16 = (long long)B * T * 3 * C / 16;
+  const int threads = 256;
+  const long long blocks = (n16 + threads - 1) / threads;
+  return launch_pdl(f8::attn_fp8_dequant, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                    static_cast<const uint4*>(codes), descale, static_cast<uint4*>(out), C, n16);
+}
+
+}  // namespace attn

@@ -80,6 +80,22 @@ attn_status_t attn_fwd_fp8(const void* qkv, const float* descale, void* out, flo
                            int NH, int causal, void* stream);
 
 /*
+ * FP8 backward: gradients of attn_fwd_fp8's attention with respect to the
+ * real q, k, v values (code * descale). The e4m3 codes are expanded to bf16
+ * on the GPU (code * descale, rounded once to bf16) and the bf16 backward
+ * (attn_bwd) runs on them: its matmuls are bf16 on the tensor core, not e4m3.
+ *   dout, out : (B, T, C) bf16 (out as attn_fwd_fp8 wrote it); lse from attn_fwd_fp8.
+ *   qkv, descale : as for attn_fwd_fp8.
+ *   dqkv : (B, T, 3C) bf16, fully overwritten with =.
+ *   workspace : attn_bwd_fp8_workspace_size(...) bytes, 256-byte aligned, caller-owned.
+ * Same shape rules as attn_fwd_fp8; no buffer may overlap another.
+ */
+size_t attn_bwd_fp8_workspace_size(int B, int T, int C, int NH, int causal);
+attn_status_t attn_bwd_fp8(const void* dout, const void* qkv, const float* descale, const void* out,
+                           const float* lse, void* dqkv, int B, int T, int C, int NH, int causal, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
  * Linear layer of the GPT-2 attention block (c_attn: x -> qkv, c_proj:
  * attention out -> y), with the bias add fused into the GEMM epilogue
  * ("LLM Systems 10 & 11: Accelerating Transformer Training and Inference"

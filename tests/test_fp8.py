@@ -1,4 +1,4 @@
-"""FP8 (e4m3) forward: attn_fwd_fp8 against the oracle on the dequantised inputs.
+"""FP8 (e4m3) forward and backward against the oracle on the dequantised inputs.
 
 The e4m3 codes stand for exact values (code * descale), so the oracle runs the
 plain float64 forward on those values. The kernel's only coarse rounding is the
@@ -11,6 +11,12 @@ most 2^-4/sqrt(3) of the value, the error of out_t,d has standard deviation at
 most sigma_t,d = sqrt((2^-4/sqrt 3)^2 sum_j att_tj^2 v_jd^2 + (2^-9/sqrt 3)^2 out_t,d^2).
 The tests check the bound and that the RMS of err / sigma stays below 1.5 (a
 misplaced code or a wrong descale gives values far above 1). lse: 1e-4 absolute.
+
+The backward (attn_bwd_fp8: the codes expanded to bf16, then the bf16 backward)
+is checked given the exact forward (bf16 rule, 2e-2 * max|ref| per q/k/v) and
+chained behind attn_fwd_fp8, where the forward's rounding reaches dq and dk
+through D = rowsum(dout * out); that test widens the rule by the propagated
+error of D, computed from the forward's measured error.
 """
 import math
 
@@ -145,3 +151,87 @@ def test_fp8_gpt2s_workload_sampled_heads(env):
     for _ in range(3):
         b, h = int(rng.integers(B)), int(rng.integers(NH))
         _check_head(g_out, g_lse, f.qkv, b, h, T, C, NH, w["causal"])
+
+
+# ----------------------------------------------------------------------------- FP8 backward
+def test_fp8_bwd_rejects_bad_arguments():
+    from causal_head_attention_fwd_gb300 import api
+    A, S = 1 << 32, 1 << 30
+    B, T, C, NH = 2, 64, 128, 2
+    n = api.attn_bwd_fp8_workspace_size(B, T, C, NH, 1)
+    assert n >= B * T * 3 * C * 2 + B * NH * T * 4
+
+    def call(**kw):
+        a = dict(dout=A, qkv=A + S, d=A + 2 * S, out=A + 3 * S, lse=A + 4 * S, dqkv=A + 5 * S, ws=A + 6 * S, n=n)
+        a.update(kw)
+        return api.attn_bwd_fp8(a["dout"], a["qkv"], a["d"], a["out"], a["lse"], a["dqkv"], B, T, C, NH, 1,
+                                a["ws"], a["n"], 0, check=False)
+    assert call(d=0) == api.ATTN_ERR_INVALID_ARG
+    assert call(n=n - 1) == api.ATTN_ERR_WORKSPACE
+    assert call(ws=0) == api.ATTN_ERR_WORKSPACE
+    assert call(ws=A + 6 * S + 16) == api.ATTN_ERR_MISALIGNED
+    assert call(dqkv=A + S + 64) == api.ATTN_ERR_INVALID_ARG         # dqkv overlaps qkv
+    assert call(ws=A + 5 * S) == api.ATTN_ERR_INVALID_ARG            # workspace overlaps dqkv
+
+
+def _bwd_fp8(env, f, out_bits, lse_f32, dout_bits, B, T, C, NH):
+    torch, api, ops = env
+    codes = torch.from_numpy(f.codes).cuda()
+    descale = torch.from_numpy(f.descale).cuda()
+    out = out_bits if isinstance(out_bits, torch.Tensor) else ops.upload(out_bits, "bf16")
+    lse = lse_f32 if isinstance(lse_f32, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(lse_f32, np.float32)).cuda()
+    dout = ops.upload(dout_bits, "bf16")
+    dqkv = torch.full((B, T, 3 * C), float("nan"), dtype=torch.bfloat16, device="cuda")
+    nws = api.attn_bwd_fp8_workspace_size(B, T, C, NH, 1)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    api.attn_bwd_fp8(dout, codes, descale, out, lse, dqkv, B, T, C, NH, 1, ws, nws)
+    torch.cuda.synchronize()
+    assert api.attn_last_device_error() == api.ATTN_OK
+    return ops.download_f64(dqkv)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,T,C,NH", [(2, 64, 128, 4), (1, 300, 128, 2), (1, 1000, 64, 1)])
+def test_fp8_backward_given_exact_forward(env, B, T, C, NH):
+    """out and lse from the oracle: the GPU backward must meet the bf16 rule (2e-2 * max|ref| per q/k/v)."""
+    f = inputs.make_fp8_inputs(B, T, C, sigma=0.5, seed=91 + T)
+    r_out, r_lse = oracle.forward(f.qkv, B, T, C, NH, True)
+    dout, dout_bits = inputs.draw((B, T, C), 1e-2, 92 + T, "bf16")
+    out_bits = inputs.f32_to_bf16_bits(r_out.astype(np.float32))
+    g = _bwd_fp8(env, f, out_bits, r_lse, dout_bits, B, T, C, NH)
+    assert np.isfinite(g).all()
+    ref = oracle.backward(dout.astype(np.float64), f.qkv, B, T, C, NH, True)
+    for sl in (slice(0, C), slice(C, 2 * C), slice(2 * C, 3 * C)):
+        assert np.max(np.abs(g[:, :, sl] - ref[:, :, sl])) <= 2e-2 * np.max(np.abs(ref[:, :, sl]))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,T,C,NH", [(1, 300, 128, 2), (2, 256, 64, 1)])
+def test_fp8_forward_then_backward(env, B, T, C, NH):
+    """The chain attn_fwd_fp8 -> attn_bwd_fp8. dv does not see the forward's rounding: bf16 rule.
+    dq, dk see it through D_t = dout_t . out_t: with dD_t the error of that sum (known here from
+    the forward's measured error), |err dq_t| <= 2e-2 max|dq| + scale |dD_t| sum_j att_tj |k_j| and
+    |err dk_j| <= 2e-2 max|dk| + scale sum_t att_tj |dD_t| |q_t|."""
+    torch, api, ops = env
+    f = inputs.make_fp8_inputs(B, T, C, sigma=0.5, seed=93 + T)
+    g_out, g_lse = _run(env, f, B, T, C, NH, 1)
+    dout, dout_bits = inputs.draw((B, T, C), 1e-2, 94 + T, "bf16")
+    out_bits = inputs.f32_to_bf16_bits(g_out.astype(np.float32))   # exact: g_out holds bf16 values
+    g = _bwd_fp8(env, f, out_bits, g_lse, dout_bits, B, T, C, NH)
+    ref = oracle.backward(dout.astype(np.float64), f.qkv, B, T, C, NH, True)
+    r_out, _ = oracle.forward(f.qkv, B, T, C, NH, True)
+    hs = C // NH
+    scale = 1.0 / math.sqrt(hs)
+    q, k, v = oracle.split_heads(f.qkv, C, NH)
+    lim = {s: 2e-2 * np.max(np.abs(ref[:, :, s * C:(s + 1) * C])) for s in range(3)}
+    for b in range(B):
+        for h in range(NH):
+            cols = slice(h * hs, (h + 1) * hs)
+            _, _, att, _ = oracle.head_forward(q[b, h], k[b, h], v[b, h], True, return_att=True)
+            dD = np.sum(dout[b, :, cols].astype(np.float64) * (g_out[b, :, cols] - r_out[b, :, cols]), axis=1)
+            tol_q = lim[0] + scale * np.abs(dD)[:, None] * (att @ np.abs(k[b, h]))
+            tol_k = lim[1] + scale * (att.T @ (np.abs(dD)[:, None] * np.abs(q[b, h])))
+            e_q = np.abs(g[b, :, cols] - ref[b, :, cols])
+            e_k = np.abs(g[b, :, C + h * hs:C + (h + 1) * hs] - ref[b, :, C + h * hs:C + (h + 1) * hs])
+            e_v = np.abs(g[b, :, 2 * C + h * hs:2 * C + (h + 1) * hs] - ref[b, :, 2 * C + h * hs:2 * C + (h + 1) * hs])
+            assert np.all(e_q <= tol_q) and np.all(e_k <= tol_k) and np.max(e_v) <= lim[2]
