@@ -29,12 +29,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id() {
-  uint32_t l;
-  asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-  return l;
-}
-
 // Per-warpgroup register budget change (all four warps of the warpgroup must
 // execute it). The increases of some warpgroups must be covered by the
 // decreases of others: the block's pool is its launch threads x registers.
@@ -335,12 +329,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// Vector fp32 reduction into global memory (16-byte aligned address).
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
-               :: "l"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
 // Programmatic dependent launch. Let the next kernel on the stream begin
