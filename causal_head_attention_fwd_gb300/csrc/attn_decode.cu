@@ -76,6 +76,35 @@ struct Chunk {
   static constexpr int N = 128;
 };
 
+// Transposing butterfly over lane masks MASK, MASK/2, ..., MASK_LO. Each lane
+// enters with N partial sums v[0..N) (the same N quantities in every lane of
+// the group). At a level with CNT > 1 live values the lane keeps the half its
+// lane bit selects, sends the other half to its partner and adds what it gets
+// back; with one live value it does a plain butterfly add. On return v[0..)
+// holds complete sums of quantities first, first + 1, ...: N / 2^levels of
+// them, or one (then shared by the lanes that differ only in the plain-add bits).
+template <int N, int CNT, int MASK, int MASK_LO>
+struct TRed {
+  static __device__ __forceinline__ void run(float (&v)[N], int lane, int& first) {
+    if constexpr (CNT > 1) {
+      constexpr int H = CNT / 2;
+      const bool hi = (lane & MASK) != 0;
+#pragma unroll
+      for (int k = 0; k < H; ++k) {
+        const float send = hi ? v[k] : v[k + H];
+        const float keep = hi ? v[k + H] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, MASK);
+      }
+      if (hi) first += H;
+      if constexpr (MASK > MASK_LO) TRed<N, H, MASK / 2, MASK_LO>::run(v, lane, first);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], MASK);
+      if constexpr (MASK > MASK_LO) TRed<N, 1, MASK / 2, MASK_LO>::run(v, lane, first);
+    }
+  }
+};
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
 // TQ: the largest Tq this instantiation serves (1, 4 or 8); its per-query
 // shared arrays and accumulators are sized by it, so the common one-token step
 // keeps more CTAs resident per SM.
@@ -88,10 +117,17 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
   constexpr int LPR = HS / 8;                 // lanes per row (8 for hs 64, 4 for hs 32)
   constexpr int GROUPS = THREADS / LPR;       // rows per CTA step
   constexpr uint32_t BYTES = CH * HS * sizeof(E);
+  // scores: TQ partial dot products reduced over the LPR lanes of a row
+  constexpr int S_LEVELS = ilog2(LPR);
+  constexpr int S_OUT = TQ >> S_LEVELS > 0 ? (TQ >> S_LEVELS) : 1;      // sums per lane afterwards
+  constexpr int S_DUP = (1 << S_LEVELS) * S_OUT / TQ;                  // lanes holding the same sum
+  // outputs: TQ x 8 partial sums reduced over the rows of a warp
+  constexpr int O_LEVELS = ilog2(32 / LPR);
+  constexpr int O_OUT = (8 * TQ) >> O_LEVELS;
+  static_assert(O_OUT >= 1, "output reduction leaves at least one value per lane");
   extern __shared__ uint8_t smem_raw[];
   E* sK = reinterpret_cast<E*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   E* sV = sK + CH * HS;
-  __shared__ __align__(16) float sq[TQ][HS];
   __shared__ float sp[TQ][CH];
   __shared__ float red[TQ][THREADS / 32];
   __shared__ float row_m[TQ];
@@ -119,38 +155,44 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
     mbar_arrive_expect_tx(&bar_v, BYTES);
     tma_load_3d(sV, &map_qkv, &bar_v, 2 * C + h * HS, j0, b);
   }
-  // the queries (last Tq positions) into shared memory, fp32
-  const size_t rs = (size_t)3 * C;
-  const E* qbase = static_cast<const E*>(p.qkv) + (size_t)b * L * rs + h * HS;
-  for (int x = tid; x < Tq * LPR; x += THREADS) {
-    const int i = x / LPR, c = (x % LPR) * 8;
-    float v[8];
-    load8<E>(qbase + (size_t)(L - Tq + i) * rs + c, v);
+  // this lane's 8 columns of the queries (the last Tq positions), in registers
+  float2 qr[TQ][4];
+  {
+    const size_t rs = (size_t)3 * C;
+    const E* qbase = static_cast<const E*>(p.qkv) + (size_t)b * L * rs + h * HS + db;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) sq[i][c + k] = v[k];
+    for (int i = 0; i < TQ; ++i) {
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (i < Tq) load8<E>(qbase + (size_t)(L - Tq + i) * rs, v);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) qr[i][k] = make_float2(v[2 * k], v[2 * k + 1]);
+    }
   }
   __syncthreads();
   bool ok = mbar_wait(&bar_k, 0, &abort_sh, p.err);
-  // scores: partial dot products over 8 columns, summed over the row's lanes
+  // scores: packed partial dot products over the lane's 8 columns, then the
+  // transposing butterfly over the row's lanes
   for (int r0 = 0; r0 < CH; r0 += GROUPS) {
     const int j = r0 + g;
     float kv[8];
     load8<E>(sK + j * HS + db, kv);
-    for (int i = 0; i < Tq; ++i) {
-      const float4 qa = *reinterpret_cast<const float4*>(&sq[i][db]);
-      const float4 qb = *reinterpret_cast<const float4*>(&sq[i][db + 4]);
-      float acc = qa.x * kv[0];
-      acc = fmaf(qa.y, kv[1], acc);
-      acc = fmaf(qa.z, kv[2], acc);
-      acc = fmaf(qa.w, kv[3], acc);
-      acc = fmaf(qb.x, kv[4], acc);
-      acc = fmaf(qb.y, kv[5], acc);
-      acc = fmaf(qb.z, kv[6], acc);
-      acc = fmaf(qb.w, kv[7], acc);
+    float part[TQ];
 #pragma unroll
-      for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if ((tid % LPR) == 0)
-        sp[i][j] = (j < nk && j0 + j <= L - Tq + i) ? acc * p.scale_log2 : -INFINITY;   // log2 units
+    for (int i = 0; i < TQ; ++i) {
+      float2 a = mul2(qr[i][0], make_float2(kv[0], kv[1]));
+      a = fma2(qr[i][1], make_float2(kv[2], kv[3]), a);
+      a = fma2(qr[i][2], make_float2(kv[4], kv[5]), a);
+      a = fma2(qr[i][3], make_float2(kv[6], kv[7]), a);
+      part[i] = a.x + a.y;
+    }
+    int first = 0;
+    if constexpr (S_LEVELS > 0) TRed<TQ, TQ, LPR / 2, 1>::run(part, lane, first);
+    if ((lane & (S_DUP - 1)) == 0) {
+#pragma unroll
+      for (int k = 0; k < S_OUT; ++k) {
+        const int i = first + k;
+        if (i < Tq) sp[i][j] = (j < nk && j0 + j <= L - Tq + i) ? part[k] * p.scale_log2 : -INFINITY;   // log2 units
+      }
     }
   }
   __syncthreads();
@@ -185,12 +227,13 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
   __syncthreads();
   ok = mbar_wait(&bar_v, 0, &abort_sh, p.err) && ok;
   // partial outputs: each lane accumulates its 8 columns over its rows of the
-  // chunk for every query, then the rows of a warp and the warps are summed
-  float acc[TQ][8];
+  // chunk for every query (packed pairs), then the transposing butterfly sums
+  // the rows of the warp and the warps are summed through shared memory
+  float2 acc[TQ][4];
 #pragma unroll
   for (int i = 0; i < TQ; ++i)
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc[i][k] = 0.f;
+    for (int k = 0; k < 4; ++k) acc[i][k] = make_float2(0.f, 0.f);
 #pragma unroll 4
   for (int r0 = 0; r0 < CH; r0 += GROUPS) {
     const int j = r0 + g;
@@ -200,25 +243,27 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
     for (int i = 0; i < TQ; ++i) {
       if (i < Tq) {
         const float pj = sp[i][j];
+        const float2 p2 = make_float2(pj, pj);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc[i][k] = fmaf(pj, vv[k], acc[i][k]);
+        for (int k = 0; k < 4; ++k) acc[i][k] = fma2(p2, make_float2(vv[2 * k], vv[2 * k + 1]), acc[i][k]);
       }
     }
   }
+  {
+    float o[8 * TQ];
 #pragma unroll
-  for (int i = 0; i < TQ; ++i) {
-    if (i < Tq) {
+    for (int i = 0; i < TQ; ++i)
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float v = acc[i][k];
-#pragma unroll
-        for (int o = LPR; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);   // rows of the warp
-        acc[i][k] = v;
+      for (int k = 0; k < 4; ++k) {
+        o[i * 8 + 2 * k] = acc[i][k].x;
+        o[i * 8 + 2 * k + 1] = acc[i][k].y;
       }
-      if (lane < LPR) {
+    int first = 0;
+    TRed<8 * TQ, 8 * TQ, 16, LPR>::run(o, lane, first);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) sacc[warp][i][db + k] = acc[i][k];
-      }
+    for (int k = 0; k < O_OUT; ++k) {
+      const int idx = first + k, i = idx / 8, dd = idx % 8;
+      if (i < Tq) sacc[warp][i][db + dd] = o[k];
     }
   }
   __syncthreads();
