@@ -32,7 +32,8 @@
 //   warp  13    MMA issuer; warps 14-15 idle
 // The softmax warpgroups copy S^T/dP^T of step g into registers and release
 // them at once, so the tensor core computes S^T/dP^T of step g+1 while P/dS of
-// step g are formed. MMA order: S(g), dP(g), dV(g-1), dK(g-1), dQ(g-1).
+// step g are formed. MMA order: S(g), dP(g), dK(g-1), dQ(g-1), dV(g-1): the dS^T
+// tile is released before dV runs, so the next one is written meanwhile.
 // TMEM columns: S^T [0,128) dP^T [128,256) P^T [256,320) dV [320,384)
 //               dK [384,448) dQ [448,512)
 #include "common.cuh"
@@ -210,7 +211,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   __shared__ uint64_t bar_kv_full[2], bar_kv_empty[2], bar_q_full[BWD_STAGES], bar_q_empty[BWD_STAGES];
-  __shared__ uint64_t bar_sdp_full, bar_sdp_free, bar_pds_full, bar_pds_free, bar_dq_full, bar_dq_free,
+  __shared__ uint64_t bar_sdp_full, bar_sdp_free, bar_pds_full, bar_ds_free, bar_p_free, bar_dq_full, bar_dq_free,
       bar_done, bar_epi_free;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
@@ -240,7 +241,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
     mbar_init(&bar_sdp_full, 1);
     mbar_init(&bar_sdp_free, 8);                 // one arrival per softmax warp
     mbar_init(&bar_pds_full, 8);
-    mbar_init(&bar_pds_free, 1);
+    mbar_init(&bar_ds_free, 1);                  // dK, dQ of the step read the dS^T tile
+    mbar_init(&bar_p_free, 1);                   // dV of the step read P^T
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_free, 4);                  // one arrival per dQ warp
     mbar_init(&bar_done, 1);
@@ -346,11 +348,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
           // dK/dV of the previous item must have been read out by its epilogue
           if (f.first && f.ic > 0 && !mbar_wait(&bar_epi_free, (f.ic - 1) & 1, &abort_sh, gerr)) return false;
           tc_fence_after();
-          // dV += P^T dO  (A = P^T in TMEM, B = dO MN-major; K = 128 queries)
-#pragma unroll
-          for (int k = 0; k < BM / 16; ++k)
-            mma_ts(tmem + TB_DV, tmem + TB_P + k * 8, desc_add(od, k * 16 * G::ROW_BYTES), id_kv,
-                   (!f.first || k > 0) ? 1u : 0u);
           // dK += dS^T Q  (A = dS^T K-major: 2 blocks of 64 queries, B = Q MN-major)
 #pragma unroll
           for (int k = 0; k < BM / 16; ++k)
@@ -366,8 +363,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
           for (int k = 0; k < BN / 16; ++k)
             mma_ss(tmem + TB_DQ, desc_add(dSm, k * 16 * 128), desc_add(kd, k * 16 * G::ROW_BYTES), id_dq, k > 0);
           mma_commit(&bar_dq_full);
-          // only commits that someone waits for (no arrival after the CTA retires)
-          if (f.g + 1 < total_g) mma_commit(&bar_pds_free);
+          // the dS^T tile is free once dK and dQ are done: the softmax warps write
+          // the next one while dV still runs (only commits that someone waits for)
+          if (f.g + 1 < total_g) mma_commit(&bar_ds_free);
+          // dV += P^T dO  (A = P^T in TMEM, B = dO MN-major; K = 128 queries)
+#pragma unroll
+          for (int k = 0; k < BM / 16; ++k)
+            mma_ts(tmem + TB_DV, tmem + TB_P + k * 8, desc_add(od, k * 16 * G::ROW_BYTES), id_kv,
+                   (!f.first || k > 0) ? 1u : 0u);
+          if (f.g + 1 < total_g) mma_commit(&bar_p_free);
           if (f.g + BWD_STAGES < total_g) mma_commit(&bar_q_empty[f.st]);
           if (f.last) {
             mma_commit(&bar_done);                           // dK/dV of item f.ic final
@@ -537,18 +541,24 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
           bwd_p_ds<true>(sv, dpv, rs, c, half * 64, r, diag, key < T, pk, dk);
         else
           bwd_p_ds<false>(sv, dpv, rs, c, half * 64, r, false, true, pk, dk);
+        // dS^T row `r`, queries [64*half, 64*half+64): block `half`, 8 chunks of
+        // 16 bytes, once the previous step's dK and dQ have read the tile
         if (g > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&bar_pds_free, (g - 1) & 1, &abort_sh, gerr));
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_ds_free, (g - 1) & 1, &abort_sh, gerr));
           if (!ok) break;
-          tc_fence_after();
         }
-        tmem_st32(tmem + lane_off + TB_P + half * 32, pk);
-        // dS^T row `r`, queries [64*half, 64*half+64): block `half`, 8 chunks of 16 bytes
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           const uint4 v = make_uint4(dk[ch * 4 + 0], dk[ch * 4 + 1], dk[ch * 4 + 2], dk[ch * 4 + 3]);
           *reinterpret_cast<uint4*>(sds + swz_chunk_offset<64>(r, ch)) = v;
         }
+        // P^T into TMEM once the previous step's dV has read it
+        if (g > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_p_free, (g - 1) & 1, &abort_sh, gerr));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        tmem_st32(tmem + lane_off + TB_P + half * 32, pk);
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
