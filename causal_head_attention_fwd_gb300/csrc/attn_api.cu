@@ -35,8 +35,8 @@ cudaError_t launch_fp8_dequant(const void* codes, const float* descale, void* ou
                                cudaStream_t stream);
 cudaError_t launch_linear(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
                           const void* bias, int M, int N, int K, cudaStream_t stream);
-cudaError_t launch_att(const CUtensorMap& map_qkv, const float* lse, float* preatt, float* att, bool f32,
-                       const Problem& pr, cudaStream_t stream);
+cudaError_t launch_att(const CUtensorMap& map_qkv, const CUtensorMap& map_pre, const CUtensorMap& map_att, bool tma_out,
+                       const float* lse, float* preatt, float* att, bool f32, const Problem& pr, cudaStream_t stream);
 
 size_t decode_workspace_bytes(int B, int L, int C, int NH, int Tq, bool f32);
 int decode_max_tq();
@@ -401,7 +401,26 @@ extern "C" attn_status_t attn_fwd_att(const void* qkv, const float* lse, float* 
                        : encode_3d(&mq, qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3 * C, T, B, pr.hs, BM,
                                    pr.hs == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (!enc) return ATTN_ERR_CUDA;
-  cudaError_t ce = launch_att(mq, lse, preatt, att, f32, pr, static_cast<cudaStream_t>(stream));
+  // the (B*NH, T, T) fp32 matrices as {T, T, B*NH} for bulk tensor stores of
+  // [128][32] chunks; row strides must be multiples of 16 bytes (T % 4 == 0)
+  CUtensorMap mp = {}, ma = {};
+  const bool tma_out = (T % 4) == 0;
+  if (tma_out) {
+    auto fn = encode_fn();
+    if (!fn) return ATTN_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)T, (cuuint64_t)T, (cuuint64_t)B * NH};
+    cuuint64_t strides[2] = {(cuuint64_t)T * 4, (cuuint64_t)T * T * 4};
+    cuuint32_t box[3] = {32, 128, 1}, es[3] = {1, 1, 1};
+    for (int i = 0; i < 2; ++i) {
+      float* base = i == 0 ? preatt : att;
+      if (!base) continue;
+      if (fn(i == 0 ? &mp : &ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return ATTN_ERR_CUDA;
+    }
+  }
+  cudaError_t ce = launch_att(mq, mp, ma, tma_out, lse, preatt, att, f32, pr, static_cast<cudaStream_t>(stream));
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

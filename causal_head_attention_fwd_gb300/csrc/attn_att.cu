@@ -11,9 +11,11 @@
 // writes
 //   preatt[b,h,t,j] = s_tj                                  (every t, j < T)
 //   att[b,h,t,j]    = exp(scale * s_tj - lse_t) if j in J(t), else 0
-// The work is bound by the HBM writes of the two T x T matrices; each 128 x 32
-// output chunk goes through shared memory so every warp store covers whole
-// 128-byte row segments.
+// The work is bound by the HBM writes of the two T x T matrices. Each 128 x 32
+// output chunk goes through shared memory: when T % 4 == 0 (16-byte row
+// strides) into a 128-byte-swizzled staging tile that one TMA bulk store
+// writes out (two tiles alternate, so a store overlaps the next chunk), else
+// into a padded tile that the warps store as whole 128-byte row segments.
 #include "../../include/attn.h"
 #include "common.cuh"
 #include "tf32.cuh"
@@ -29,7 +31,9 @@ struct Smem {
   static constexpr int TILE = F32 ? HS * 128 * 4 : HS * 128 * 2;
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = TILE;
-  static constexpr int ALLOC = 2 * TILE + 1024;
+  static constexpr int STG_OFF = 2 * TILE;               // two [128][32] fp32 staging tiles, 128-byte swizzle
+  static constexpr int STG_BYTES = 128 * 128;
+  static constexpr int ALLOC = STG_OFF + 2 * STG_BYTES + 1024;
 };
 
 struct Params {
@@ -41,14 +45,15 @@ struct Params {
   float scale_log2;
 };
 
-template <bool F32, int HS, bool CAUSAL>
+template <bool F32, int HS, bool CAUSAL, bool TMA_OUT>
 __global__ void __launch_bounds__(THREADS)
-attn_att_kernel(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
+attn_att_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_pre,
+                const __grid_constant__ CUtensorMap map_att, const Params p) {
   using L = Smem<F32, HS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_ld, bar_mma;
-  __shared__ float stage[BM][33];        // one 128 x 32 fp32 output chunk, padded
+  __shared__ float stage[TMA_OUT ? 1 : BM][33];   // plain-store path: one 128 x 32 fp32 chunk, padded
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
 
@@ -121,8 +126,9 @@ attn_att_kernel(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
   if (ok) {
     const float lse2 = t < T ? p.lse[(size_t)bh * T + t] * 1.4426950408889634f : 0.f;
     const float c = p.scale_log2;
-    const bool vec = (T & 3) == 0;             // global rows start 16-byte aligned
     float* mats[2] = {p.preatt, p.att};
+    const CUtensorMap* maps[2] = {&map_pre, &map_att};
+    int n = 0;                                   // chunks staged so far (TMA path)
 #pragma unroll 1
     for (int cc = 0; cc < BN; cc += 32) {
       uint32_t s[32];
@@ -134,25 +140,45 @@ attn_att_kernel(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
       for (int m = 0; m < 2; ++m) {
         float* dst = mats[m];
         if (!dst) continue;                        // uniform: the same pointer for every thread
-        // thread = row writes its 32 values into a padded [128][33] tile
-        // (conflict-free), then each warp stores whole 128-byte row segments
-        __syncthreads();
+        if constexpr (TMA_OUT) {
+          // row r's 32 values into a [128][32] fp32 staging tile (128-byte
+          // swizzle), then one bulk tensor store; two tiles alternate
+          uint8_t* stg = smem + L::STG_OFF + (n & 1) * L::STG_BYTES;
+          if (threadIdx.x == 0) bulk_wait_group_read1();   // the store two chunks ago has read this tile
+          __syncthreads();
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          stage[r][e] = m == 0 ? __uint_as_float(s[e])
-                               : (e < nvis ? ex2_approx(__uint_as_float(s[e]) * c - lse2) : 0.f);
-        __syncthreads();
+          for (int ch = 0; ch < 8; ++ch) {
+            float v[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int i = k * THREADS + r;           // [128 rows][8 float4] of the chunk
-          const int rr = i >> 3, c4 = (i & 7) * 4;
-          const int tg = qt * BM + rr, jg = j0 + c4;
-          if (tg >= T || jg >= T) continue;
-          float* g = dst + ((size_t)bh * T + tg) * (size_t)T + jg;
-          if (vec) {
-            *reinterpret_cast<float4*>(g) = make_float4(stage[rr][c4], stage[rr][c4 + 1], stage[rr][c4 + 2],
-                                                        stage[rr][c4 + 3]);
-          } else {
+            for (int k = 0; k < 4; ++k) {
+              const int e = ch * 4 + k;
+              v[k] = m == 0 ? __uint_as_float(s[e]) : (e < nvis ? ex2_approx(__uint_as_float(s[e]) * c - lse2) : 0.f);
+            }
+            *reinterpret_cast<float4*>(stg + r * 128 + ((ch ^ (r & 7)) << 4)) = make_float4(v[0], v[1], v[2], v[3]);
+          }
+          fence_proxy_async_smem();
+          __syncthreads();
+          if (threadIdx.x == 0) {
+            tma_store_3d(maps[m], stg, j0, qt * BM, bh);
+            bulk_commit_group();
+          }
+          ++n;
+        } else {
+          // thread = row writes its 32 values into a padded [128][33] tile
+          // (conflict-free), then each warp stores whole 128-byte row segments
+          __syncthreads();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            stage[r][e] = m == 0 ? __uint_as_float(s[e])
+                                 : (e < nvis ? ex2_approx(__uint_as_float(s[e]) * c - lse2) : 0.f);
+          __syncthreads();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int i = k * THREADS + r;           // [128 rows][8 float4] of the chunk
+            const int rr = i >> 3, c4 = (i & 7) * 4;
+            const int tg = qt * BM + rr, jg = j0 + c4;
+            if (tg >= T || jg >= T) continue;
+            float* g = dst + ((size_t)bh * T + tg) * (size_t)T + jg;
 #pragma unroll
             for (int x = 0; x < 4; ++x)
               if (jg + x < T) g[x] = stage[rr][c4 + x];
@@ -160,27 +186,41 @@ attn_att_kernel(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
         }
       }
     }
+    if constexpr (TMA_OUT) {
+      if (threadIdx.x == 0) bulk_wait_group0();   // every store complete before the CTA retires
+    }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
-template <bool F32, int HS, bool CAUSAL>
-static cudaError_t launch_t(const CUtensorMap& m, const Params& p, cudaStream_t s) {
-  auto k = attn_att_kernel<F32, HS, CAUSAL>;
+template <bool F32, int HS, bool CAUSAL, bool TMA_OUT>
+static cudaError_t launch_t(const CUtensorMap& m, const CUtensorMap& mp, const CUtensorMap& ma, const Params& p,
+                            cudaStream_t s) {
+  auto k = attn_att_kernel<F32, HS, CAUSAL, TMA_OUT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<F32, HS>::ALLOC);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)p.BH * p.n_tiles * p.n_tiles;
-  k<<<(unsigned)grid, THREADS, Smem<F32, HS>::ALLOC, s>>>(m, p);
+  k<<<(unsigned)grid, THREADS, Smem<F32, HS>::ALLOC, s>>>(m, mp, ma, p);
   return cudaGetLastError();
+}
+
+template <bool F32, int HS>
+static cudaError_t launch_hs(const CUtensorMap& m, const CUtensorMap& mp, const CUtensorMap& ma, const Params& p,
+                             bool causal, bool tma, cudaStream_t s) {
+  if (tma)
+    return causal ? launch_t<F32, HS, true, true>(m, mp, ma, p, s) : launch_t<F32, HS, false, true>(m, mp, ma, p, s);
+  return causal ? launch_t<F32, HS, true, false>(m, mp, ma, p, s) : launch_t<F32, HS, false, false>(m, mp, ma, p, s);
 }
 
 }  // namespace attk
 
-// map_qkv: qkv as {3C, T, B}, box {hs, 128} (bf16) or {32, 128} (fp32)
-cudaError_t launch_att(const CUtensorMap& map_qkv, const float* lse, float* preatt, float* att, bool f32,
-                       const Problem& pr, cudaStream_t stream) {
+// map_qkv: qkv as {3C, T, B}, box {hs, 128} (bf16) or {32, 128} (fp32);
+// map_pre / map_att: the fp32 matrices as {T, T, B*NH}, box {32, 128, 1},
+// 128-byte swizzle, used when tma_out (T % 4 == 0) and the matrix is wanted.
+cudaError_t launch_att(const CUtensorMap& map_qkv, const CUtensorMap& map_pre, const CUtensorMap& map_att, bool tma_out,
+                       const float* lse, float* preatt, float* att, bool f32, const Problem& pr, cudaStream_t stream) {
   attk::Params p;
   p.lse = lse;
   p.preatt = preatt;
@@ -192,18 +232,12 @@ cudaError_t launch_att(const CUtensorMap& map_qkv, const float* lse, float* prea
   p.BH = pr.B * pr.NH;
   p.n_tiles = (pr.T + BM - 1) / BM;
   p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)pr.hs));
-  if (f32) {
-    if (pr.hs == 64)
-      return pr.causal ? attk::launch_t<true, 64, true>(map_qkv, p, stream)
-                       : attk::launch_t<true, 64, false>(map_qkv, p, stream);
-    return pr.causal ? attk::launch_t<true, 32, true>(map_qkv, p, stream)
-                     : attk::launch_t<true, 32, false>(map_qkv, p, stream);
-  }
-  if (pr.hs == 64)
-    return pr.causal ? attk::launch_t<false, 64, true>(map_qkv, p, stream)
-                     : attk::launch_t<false, 64, false>(map_qkv, p, stream);
-  return pr.causal ? attk::launch_t<false, 32, true>(map_qkv, p, stream)
-                   : attk::launch_t<false, 32, false>(map_qkv, p, stream);
+  const bool c = pr.causal != 0;
+  if (f32)
+    return pr.hs == 64 ? attk::launch_hs<true, 64>(map_qkv, map_pre, map_att, p, c, tma_out, stream)
+                       : attk::launch_hs<true, 32>(map_qkv, map_pre, map_att, p, c, tma_out, stream);
+  return pr.hs == 64 ? attk::launch_hs<false, 64>(map_qkv, map_pre, map_att, p, c, tma_out, stream)
+                     : attk::launch_hs<false, 32>(map_qkv, map_pre, map_att, p, c, tma_out, stream);
 }
 
 }  // namespace attn
