@@ -677,7 +677,8 @@ def main(argv=None):
 
 # CUDA sources each kernel is compiled from (its translation unit and headers)
 _KERNEL_SOURCES = {
-    "bf16": ["attn_fwd.cu", "attn_bwd.cu", "common.cuh", "ptx.cuh"],
+    "attn_fwd_kernel": ["attn_fwd.cu", "common.cuh", "ptx.cuh"],
+    "attn_bwd_kernel": ["attn_bwd.cu", "common.cuh", "ptx.cuh"],
     "f32": ["attn_f32.cu", "tf32.cuh", "common.cuh", "ptx.cuh"],
 }
 
@@ -688,7 +689,10 @@ def kernel_source_hash(kernel: str = "attn_bwd_kernel") -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = ROOT / "causal_head_attention_fwd_gb300" / "csrc"
-    for name in _KERNEL_SOURCES["f32" if "f32" in kernel else "bf16"]:
+    names = _KERNEL_SOURCES.get("f32" if "f32" in kernel else kernel)
+    if names is None:
+        return ""
+    for name in names:
         h.update(name.encode())
         h.update((csrc / name).read_bytes())
     return h.hexdigest()[:16]
