@@ -41,7 +41,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, C % NH != 0, aliasing */
-  ATTN_ERR_UNSUPPORTED = 2,   /* head size or dtype this build does not implement */
+  ATTN_ERR_UNSUPPORTED = 2,   /* head size or dtype the library does not implement */
   ATTN_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
   ATTN_ERR_WORKSPACE = 4,     /* backward workspace missing or too small */
   ATTN_ERR_CUDA = 5,          /* a CUDA runtime/driver call or launch failed */
