@@ -342,7 +342,12 @@ extern "C" attn_status_t attn_bwd(const void* dout, const void* qkv, const void*
   const size_t e = esize(dtype);
   const size_t n3 = (size_t)B * T * 3 * C * e, n1 = (size_t)B * T * C * e, nl = (size_t)B * NH * T * 4;
   if (overlaps(dqkv, n3, qkv, n3) || overlaps(dqkv, n3, out, n1) || overlaps(dqkv, n3, dout, n1) ||
-      overlaps(dqkv, n3, lse, nl) || (workspace && overlaps(dqkv, n3, workspace, need)))
+      overlaps(dqkv, n3, lse, nl))
+    return ATTN_ERR_INVALID_ARG;
+  // the workspace (D and the dq accumulator) is written: it may share no byte with any other buffer
+  if (workspace && (overlaps(workspace, need, dqkv, n3) || overlaps(workspace, need, qkv, n3) ||
+                    overlaps(workspace, need, out, n1) || overlaps(workspace, need, dout, n1) ||
+                    overlaps(workspace, need, lse, nl)))
     return ATTN_ERR_INVALID_ARG;
   Problem pr{B, T, C, NH, C / NH, causal};
   if (!device_error_word() || device_sm_count() <= 0) return ATTN_ERR_CUDA;

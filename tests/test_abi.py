@@ -83,6 +83,9 @@ def test_fwd_rejects_bad_arguments(api, kw, expect):
     (dict(dqkv=0), "INVALID_ARG"), (dict(dqkv=A + 4 * S + 8), "MISALIGNED"),
     (dict(ws=0), "WORKSPACE"), (dict(wsb=1024), "WORKSPACE"), (dict(ws=A + 5 * S + 128), "MISALIGNED"),
     (dict(dqkv=A + S + 4096), "INVALID_ARG"), (dict(dqkv=A), "INVALID_ARG"),
+    # the workspace is written, so it may not overlap any input or dqkv
+    (dict(ws=A + 4 * S), "INVALID_ARG"), (dict(ws=A + 256), "INVALID_ARG"), (dict(ws=A + S), "INVALID_ARG"),
+    (dict(ws=A + 2 * S + 256), "INVALID_ARG"), (dict(ws=A + 3 * S), "INVALID_ARG"),
 ])
 def test_bwd_rejects_bad_arguments(api, kw, expect):
     st = _bwd(api, **kw)
