@@ -29,7 +29,7 @@ EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_status_stri
             "attn_last_device_error", "attn_profile_enable", "attn_profile_reset",
             "attn_profile_read", "attn_bwd_noalloc", "attn_selftest_wait_timeout", "attn_fwd_att",
             "attn_decode_workspace_size", "attn_decode", "attn_fwd_fp8", "attn_linear_fwd",
-            "attn_bwd_fp8_workspace_size", "attn_bwd_fp8")
+            "attn_bwd_fp8_workspace_size", "attn_bwd_fp8", "attn_fwd_schedule")
 
 # size of the fixed scratch array attn_bwd_noalloc uses (ATTN_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -90,6 +90,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_bwd_fp8_workspace_size.restype = sz
     lib.attn_bwd_fp8.argtypes = [vp, vp, f_p, vp, f_p, vp, i, i, i, i, i, vp, sz, vp]
     lib.attn_bwd_fp8.restype = i
+    lib.attn_fwd_schedule.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int), i]
+    lib.attn_fwd_schedule.restype = i
     return lib
 
 
@@ -207,6 +209,22 @@ def attn_linear_fwd(inp, weight, bias, out, M, N, K, stream=None, check=True) ->
     if check and st != ATTN_OK:
         raise AttnError(st, "attn_linear_fwd")
     return st
+
+
+def attn_fwd_schedule(B, T, C, NH, n_cta):
+    """The forward's causal deal of work items over min(items, n_cta) CTAs:
+    (off, items) int lists, CTA c running items[off[c]:off[c+1]]; None when the
+    forward uses its snake order for this shape."""
+    n_items = B * NH * ((T + 255) // 256)
+    grid = min(n_items, n_cta)
+    off = (ctypes.c_int * (grid + 1))()
+    items = (ctypes.c_int * max(n_items, 1))()
+    n = _lib.attn_fwd_schedule(B, T, C, NH, n_cta, off, items, n_items)
+    if n < 0:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "attn_fwd_schedule")
+    if n == 0:
+        return None
+    return list(off), list(items)[:n]
 
 
 def attn_selftest_wait_timeout(limit_us: int, stream=None) -> int:

@@ -22,6 +22,7 @@ cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_d
                             const CUtensorMap& map_dqkv, const CUtensorMap& map_dqacc, const void* dout,
                             const void* out, const float* lse, void* dqkv, float* ws_D, float* ws_dq,
                             const Problem& pr, cudaStream_t stream);
+int fwd_schedule(const Problem& pr, int n_cta, int* off, int* items, int cap);
 cudaError_t launch_fwd_f32(const CUtensorMap& map_q_l, const CUtensorMap& map_q_s, const CUtensorMap& map_out_l,
                            float* lse, const Problem& pr, cudaStream_t stream);
 cudaError_t launch_bwd_f32(const CUtensorMap& map_q_l, const CUtensorMap& map_q_s, const CUtensorMap& map_do_l,
@@ -231,6 +232,12 @@ extern "C" attn_status_t attn_fwd(const void* qkv, void* out, float* lse, int B,
     return ATTN_ERR_CUDA;
   cudaError_t ce = launch_fwd_bf16(mq, mo, lse, pr, static_cast<cudaStream_t>(stream));
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" int attn_fwd_schedule(int B, int T, int C, int NH, int n_cta, int* off, int* items, int cap) {
+  if (check_shape(B, T, C, NH, 1, ATTN_BF16) != ATTN_OK || n_cta < 1 || !off || !items || cap < 0) return -1;
+  Problem pr{B, T, C, NH, C / NH, 1};
+  return fwd_schedule(pr, n_cta, off, items, cap);
 }
 
 extern "C" attn_status_t attn_fwd_fp8(const void* qkv, const float* descale, void* out, float* lse, int B, int T,

@@ -214,6 +214,23 @@ attn_status_t attn_bwd_noalloc(const void* dout, const void* qkv, const void* ou
                                attn_dtype_t dtype, void* stream);
 
 /*
+ * The forward's deal of causal work items over its CTAs, for inspection and
+ * tests (scheduling is not on the pages). A work item is two 128-row query
+ * tiles of one head: item i covers query rows from 256*(P-1-i/(B*NH)) of head
+ * i%(B*NH) (b = head/NH, h = head%NH), where P = ceil(T/256), so low indices
+ * are the long causal rows. attn_fwd deals the items longest first, each to
+ * the CTA with the least work so far (an item weighs its key tiles plus 1.7
+ * for its start-up), over G = min(items, n_cta) CTAs, one per SM.
+ *   off   : G+1 ints: CTA c runs items[off[c] .. off[c+1]) in that order.
+ *   items : cap ints.
+ * Returns the item count B*NH*P, 0 if attn_fwd uses no table for this shape
+ * (more than 2048 items or more than 160 CTAs: then CTA c takes items
+ * c, 2G-1-c, 2G+c, ... in rounds of G), or -1 for invalid arguments (shape as
+ * for attn_fwd, n_cta < 1, null arrays, cap too small). No device access.
+ */
+int attn_fwd_schedule(int B, int T, int C, int NH, int n_cta, int* off, int* items, int cap);
+
+/*
  * Failure-detection self-test (no counterpart on the pages). Launches one warp
  * that waits, with the bounded-wait mechanism every kernel of this library
  * uses, on an mbarrier phase nothing completes; after limit_us microseconds
