@@ -677,7 +677,7 @@ def main(argv=None):
 
 # CUDA sources each kernel is compiled from (its translation unit and headers)
 _KERNEL_SOURCES = {
-    "attn_fwd_kernel": ["attn_fwd.cu", "common.cuh", "ptx.cuh"],
+    "attn_fwd_kernel": ["attn_fwd.cu", "fwd_deal.cuh", "common.cuh", "ptx.cuh"],
     "attn_bwd_kernel": ["attn_bwd.cu", "common.cuh", "ptx.cuh"],
     "f32": ["attn_f32.cu", "tf32.cuh", "common.cuh", "ptx.cuh"],
 }

@@ -27,13 +27,8 @@
 // a TMA store while the next item's first scores are computed.
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+HS) O1 [320,320+HS)
 //               P0 [384,448) P1 [448,512)  (P = bf16 pairs, 64 columns)
-#include <algorithm>
-#include <functional>
-#include <mutex>
-#include <queue>
-#include <vector>
-
 #include "common.cuh"
+#include "fwd_deal.cuh"
 
 namespace attn {
 
@@ -70,27 +65,8 @@ struct FwdItem {
   int n_max;
 };
 
-// Causal work items differ in length (2 to 2*ceil(T/256) key steps); the host
-// deals them to the CTAs longest first, each to the CTA with the least work so
-// far, and passes the lists in the launch parameters. Without a table (too
-// many items, or equal items when non-causal) a CTA takes rounds of gridDim.x
-// items in snake order.
-constexpr int FWD_SCHED_MAX_ITEMS = 2048, FWD_SCHED_MAX_CTAS = 160;
-struct FwdSched {
-  int use;
-  uint16_t off[FWD_SCHED_MAX_CTAS + 1];    // CTA c's items: item[off[c] .. off[c+1])
-  uint16_t item[FWD_SCHED_MAX_ITEMS];
-};
-
-// Work item k of this CTA.
-__device__ __forceinline__ int fwd_item(const FwdSched& s, int k) {
-  const int G = gridDim.x, c = blockIdx.x;
-  if (s.use) return s.item[s.off[c] + k];
-  return k * G + ((k & 1) ? (G - 1 - c) : c);
-}
-
 template <bool CAUSAL>
-__host__ __device__ __forceinline__ FwdItem fwd_decode(int idx, const FwdParams& p) {
+__device__ __forceinline__ FwdItem fwd_decode(int idx, const FwdParams& p) {
   FwdItem w;
   const int pair = p.n_pairs - 1 - idx / p.BH;   // late (long causal rows) pairs first
   const int bh = idx % p.BH;
@@ -110,7 +86,7 @@ template <int HS, bool CAUSAL>
 __global__ void __launch_bounds__(FWD_THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
                 const __grid_constant__ CUtensorMap map_out, const FwdParams p,
-                const __grid_constant__ FwdSched sched) {
+                const __grid_constant__ WorkDeal sched) {
   using G = TileGeom<HS>;
   using L = FwdSmem<HS>;
   extern __shared__ uint8_t smem_raw[];
@@ -126,18 +102,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
   const int lane = threadIdx.x & 31;
   const int T = p.T;
   // this CTA's items and its total number of key-tile steps
-  int n_items_cta = 0, total_kv = 0;
-  if (sched.use) {
-    n_items_cta = sched.off[blockIdx.x + 1] - sched.off[blockIdx.x];
-    for (int k = 0; k < n_items_cta; ++k) total_kv += fwd_decode<CAUSAL>(fwd_item(sched, k), p).n_max;
-  } else {
-    for (int k = 0;; ++k) {
-      const int idx = fwd_item(sched, k);
-      if (idx >= p.n_items) break;
-      ++n_items_cta;
-      total_kv += fwd_decode<CAUSAL>(idx, p).n_max;
-    }
-  }
+  const int n_items_cta = deal_count(sched, p.n_items);
+  int total_kv = 0;
+  for (int k = 0; k < n_items_cta; ++k) total_kv += fwd_decode<CAUSAL>(deal_item(sched, k), p).n_max;
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
@@ -178,7 +145,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
       bool ok = true;
       int gk = 0;                                 // key-tile steps so far
       for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-        const FwdItem w = fwd_decode<CAUSAL>(fwd_item(sched, ic), p);
+        const FwdItem w = fwd_decode<CAUSAL>(deal_item(sched, ic), p);
         const int qb = ic & 1;
         if (ic >= 2 && !(ok = mbar_wait(&bar_q_empty[qb], ((ic >> 1) - 1) & 1, &abort_sh, gerr))) break;
         const uint32_t qbytes = (w.n_tile[0] > 0 ? G::TILE_BYTES : 0) + (w.n_tile[1] > 0 ? G::TILE_BYTES : 0);
@@ -231,7 +198,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
       int gk = 0;                                 // key-tile steps so far
       int gs = 0;                                 // softmax steps of this query tile so far
       for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-        const FwdItem w = fwd_decode<CAUSAL>(fwd_item(sched, ic), p);
+        const FwdItem w = fwd_decode<CAUSAL>(deal_item(sched, ic), p);
         const int qb = ic & 1;
         const int n = w.n_tile[i];
         // first scores of the item, once the softmax warps hold the previous S_i
@@ -284,7 +251,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
     bool ok = true;
     int gs = 0;                                  // softmax steps of this tile so far
     for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-      const FwdItem w = fwd_decode<CAUSAL>(fwd_item(sched, ic), p);
+      const FwdItem w = fwd_decode<CAUSAL>(deal_item(sched, ic), p);
       const int qb = ic & 1;
       const int n = w.n_tile[wg];
       const int t = w.q0 + wg * BM + r;          // query row
@@ -434,7 +401,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
 // ----------------------------------------------------------------------------
 template <int HS, bool CAUSAL>
 static cudaError_t launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mo, const FwdParams& p,
-                                const FwdSched& sc, int grid, cudaStream_t stream) {
+                                const WorkDeal& sc, int grid, cudaStream_t stream) {
   auto k = attn_fwd_kernel<HS, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdSmem<HS>::ALLOC);
   if (e != cudaSuccess) return e;
@@ -442,49 +409,17 @@ static cudaError_t launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mo, co
   return launch_pdl(k, dim3(grid), dim3(FWD_THREADS), FwdSmem<HS>::ALLOC, stream, mq, mo, p, sc);
 }
 
-// Longest-processing-time deal of the causal work items over `grid` CTAs. An
-// item costs its key steps plus ~1.7 steps for the item boundary (measured:
-// ~4k cycles between an item's last P and the next item's first scores,
-// against ~2.4k per step). Item indices run longest first.
-static void build_fwd_sched(FwdSched& s, const FwdParams& p, int grid) {
-  s.use = 0;
-  if (p.n_items > FWD_SCHED_MAX_ITEMS || grid > FWD_SCHED_MAX_CTAS) return;
-  using Load = std::pair<float, int>;      // (work so far, CTA): least work, then lowest CTA
-  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-  for (int c = 0; c < grid; ++c) heap.push({0.f, c});
-  std::vector<std::vector<int>> per(grid);
-  for (int idx = 0; idx < p.n_items; ++idx) {
-    const Load l = heap.top();
-    heap.pop();
-    per[l.second].push_back(idx);
-    heap.push({l.first + (float)fwd_decode<true>(idx, p).n_max + 1.7f, l.second});
-  }
-  int n = 0;
-  for (int c = 0; c < grid; ++c) {
-    s.off[c] = (uint16_t)n;
-    for (int idx : per[c]) s.item[n++] = (uint16_t)idx;
-  }
-  s.off[grid] = (uint16_t)n;
-  s.use = 1;
-}
-
 // The causal deal as plain arrays (see attn_fwd_schedule); 0 without a table.
 int fwd_schedule(const Problem& pr, int n_cta, int* off, int* items, int cap) {
-  FwdParams p{};
-  p.T = pr.T;
-  p.NH = pr.NH;
-  p.C = pr.C;
-  p.n_pairs = (pr.T + 2 * BM - 1) / (2 * BM);
-  p.BH = pr.B * pr.NH;
-  p.n_items = p.n_pairs * p.BH;
-  const int grid = p.n_items < n_cta ? p.n_items : n_cta;
-  static thread_local FwdSched s;
-  build_fwd_sched(s, p, grid);
+  const int n_pairs = (pr.T + 2 * BM - 1) / (2 * BM), BH = pr.B * pr.NH, n_items = n_pairs * BH;
+  const int grid = n_items < n_cta ? n_items : n_cta;
+  static thread_local WorkDeal s;
+  build_causal_deal(s, n_pairs, BH, pr.T, grid);
   if (!s.use) return 0;
-  if (cap < p.n_items) return -1;
+  if (cap < n_items) return -1;
   for (int c = 0; c <= grid; ++c) off[c] = s.off[c];
-  for (int k = 0; k < p.n_items; ++k) items[k] = s.item[k];
-  return p.n_items;
+  for (int k = 0; k < n_items; ++k) items[k] = s.item[k];
+  return n_items;
 }
 
 cudaError_t launch_fwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_out, float* lse,
@@ -501,22 +436,7 @@ cudaError_t launch_fwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_o
   p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)pr.hs));
   const int n_sm = device_sm_count();
   const int grid = p.n_items < n_sm ? p.n_items : n_sm;   // persistent: one CTA per SM
-  // the causal deal depends only on (items, heads, T, grid): built once per shape
-  static std::mutex mu;
-  static FwdSched cached;
-  static long long cached_key[4] = {-1, -1, -1, -1};
-  FwdSched sc;
-  if (pr.causal) {
-    std::lock_guard<std::mutex> lk(mu);
-    const long long key[4] = {p.n_items, p.BH, p.T, grid};
-    if (!std::equal(key, key + 4, cached_key)) {
-      build_fwd_sched(cached, p, grid);
-      std::copy(key, key + 4, cached_key);
-    }
-    sc = cached;
-  } else {
-    sc.use = 0;
-  }
+  const WorkDeal sc = launch_deal(pr.causal, p.n_pairs, p.BH, p.T, grid);
   if (pr.hs == 64)
     return pr.causal ? launch_fwd_t<64, true>(map_qkv, map_out, p, sc, grid, stream)
                      : launch_fwd_t<64, false>(map_qkv, map_out, p, sc, grid, stream);

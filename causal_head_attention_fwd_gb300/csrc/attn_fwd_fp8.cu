@@ -15,7 +15,8 @@
 // Same schedule as the bf16 forward (attention forward_cpu passes 1-4 of
 // llm.c dev/cuda/attention_backward.cu, in the FlashAttention form of
 // "Umakini wa kujitegemea, kerneli za CUDA na FlashAttention" section 3):
-// persistent CTAs, work item = two 128-row query tiles of one (b, h), 12 warps
+// persistent CTAs, work item = two 128-row query tiles of one (b, h), items
+// dealt longest first as in fwd_deal.cuh, 12 warps
 //   warps 0-3 / 4-7  softmax warpgroups of query tiles 0 / 1 (TMEM lanes)
 //   warp  8          TMA producer (Q per item, K/V through a ring)
 //   warps 9-10       MMA issuers, one per query tile; warp 11 idle
@@ -25,6 +26,7 @@
 //               P0 [384,416) P1 [416,448)
 #include "../../include/attn.h"
 #include "common.cuh"
+#include "fwd_deal.cuh"
 
 namespace attn {
 namespace f8 {
@@ -102,11 +104,6 @@ struct Item {
   int n_max;
 };
 
-__device__ __forceinline__ int item_index(int k) {
-  const int G = gridDim.x, c = blockIdx.x;
-  return k * G + ((k & 1) ? (G - 1 - c) : c);
-}
-
 template <bool CAUSAL>
 __device__ __forceinline__ Item decode(int idx, const Params& p) {
   Item w;
@@ -127,7 +124,7 @@ __device__ __forceinline__ Item decode(int idx, const Params& p) {
 template <int HS, bool CAUSAL>
 __global__ void __launch_bounds__(THREADS, 1)
 attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_out,
-                    const Params p) {
+                    const Params p, const __grid_constant__ WorkDeal deal) {
   using G = Geom<HS>;
   using L = Smem<HS>;
   extern __shared__ uint8_t smem_raw[];
@@ -142,13 +139,10 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int T = p.T;
-  int n_items_cta = 0, total_kv = 0;
-  for (int k = 0;; ++k) {
-    const int idx = item_index(k);
-    if (idx >= p.n_items) break;
-    ++n_items_cta;
-    total_kv += decode<CAUSAL>(idx, p).n_max;
-  }
+  // this CTA's items (longest first) and its total number of key-tile steps
+  const int n_items_cta = deal_count(deal, p.n_items);
+  int total_kv = 0;
+  for (int k = 0; k < n_items_cta; ++k) total_kv += decode<CAUSAL>(deal_item(deal, k), p).n_max;
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
@@ -188,7 +182,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
         bool ok = true;
         int gk = 0;
         for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-          const Item w = decode<CAUSAL>(item_index(ic), p);
+          const Item w = decode<CAUSAL>(deal_item(deal, ic), p);
           const int qb = ic & 1;
           if (ic >= 2 && !(ok = mbar_wait(&bar_q_empty[qb], ((ic >> 1) - 1) & 1, &abort_sh, gerr))) break;
           const uint32_t qbytes = (w.n_tile[0] > 0 ? G::TILE_BYTES : 0) + (w.n_tile[1] > 0 ? G::TILE_BYTES : 0);
@@ -238,7 +232,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
         bool ok = true;
         int gk = 0, gs = 0;
         for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-          const Item w = decode<CAUSAL>(item_index(ic), p);
+          const Item w = decode<CAUSAL>(deal_item(deal, ic), p);
           const int qb = ic & 1;
           const int n = w.n_tile[i];
           if (n > 0) {
@@ -289,7 +283,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
     bool ok = true;
     int gs = 0;
     for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-      const Item w = decode<CAUSAL>(item_index(ic), p);
+      const Item w = decode<CAUSAL>(deal_item(deal, ic), p);
       const int qb = ic & 1;
       const int n = w.n_tile[wg];
       const int t = w.q0 + wg * BM + r;
@@ -429,13 +423,13 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
 }
 
 template <int HS, bool CAUSAL>
-static cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mo, const Params& p, int grid,
-                            cudaStream_t stream) {
+static cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mo, const Params& p, const WorkDeal& deal,
+                            int grid, cudaStream_t stream) {
   auto k = attn_fwd_fp8_kernel<HS, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<HS>::ALLOC);
   if (e != cudaSuccess) return e;
   ProfileScope ps(K_FWD, stream);
-  k<<<grid, THREADS, Smem<HS>::ALLOC, stream>>>(mq, mo, p);
+  k<<<grid, THREADS, Smem<HS>::ALLOC, stream>>>(mq, mo, p, deal);
   return cudaGetLastError();
 }
 
@@ -458,11 +452,12 @@ cudaError_t launch_fwd_fp8(const CUtensorMap& map_qkv, const CUtensorMap& map_ou
   p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)pr.hs));
   const int n_sm = device_sm_count();
   const int grid = p.n_items < n_sm ? p.n_items : n_sm;
+  const WorkDeal deal = launch_deal(pr.causal, p.n_pairs, p.BH, p.T, grid);
   if (pr.hs == 64)
-    return pr.causal ? f8::launch_t<64, true>(map_qkv, map_out, p, grid, stream)
-                     : f8::launch_t<64, false>(map_qkv, map_out, p, grid, stream);
-  return pr.causal ? f8::launch_t<32, true>(map_qkv, map_out, p, grid, stream)
-                   : f8::launch_t<32, false>(map_qkv, map_out, p, grid, stream);
+    return pr.causal ? f8::launch_t<64, true>(map_qkv, map_out, p, deal, grid, stream)
+                     : f8::launch_t<64, false>(map_qkv, map_out, p, deal, grid, stream);
+  return pr.causal ? f8::launch_t<32, true>(map_qkv, map_out, p, deal, grid, stream)
+                   : f8::launch_t<32, false>(map_qkv, map_out, p, deal, grid, stream);
 }
 
 }  // namespace attn
