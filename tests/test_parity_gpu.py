@@ -77,7 +77,7 @@ def _run(env, B, T, C, NH, causal, dtype="bf16", sq=0.5, sd=1e-2, seed=0):
 
 SHAPES = [
     # B, T, C, NH, causal         (hs = C/NH; T spans one tile, several tiles, ragged tails)
-    (1, 1, 128, 2, 1), (1, 1, 128, 2, 0),
+    (1, 1, 128, 2, 1), (1, 1, 128, 2, 0), (2, 2, 128, 2, 1),
     (2, 17, 128, 2, 1), (2, 64, 128, 4, 1), (2, 127, 64, 1, 0),
     (1, 128, 128, 2, 1), (1, 129, 128, 4, 1), (2, 196, 128, 2, 0),
     (1, 255, 64, 1, 1), (1, 256, 64, 1, 0), (1, 257, 64, 1, 1),
