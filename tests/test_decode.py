@@ -4,7 +4,7 @@ The oracle computes the full causal forward over all L positions; the decode
 step's outputs must equal its last Tq rows (out and lse), since query i sits
 at position L-Tq+i and sees keys 0..L-Tq+i. The decode kernels compute in fp32
 from the stored inputs (no reduced-precision products), so fp32 inputs match
-to 2e-3 of max|out| (spec fp32 rule; observed ~1e-6) and bf16 inputs to
+to 2e-3 of max|out| (the fp32 parity rule; observed ~1e-6) and bf16 inputs to
 2e-2 (the bf16 output rounding dominates); lse to 1e-4 absolute.
 """
 import numpy as np
