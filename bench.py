@@ -141,19 +141,23 @@ import oracle
 from causal_head_attention_fwd_gb300 import inputs
 w = inputs.WORKLOADS[sys.argv[2]]
 budget = float(sys.argv[3]); max_heads = int(sys.argv[4])
-x, _ = inputs.draw((1, w.T, 3 * w.C), w.sigma_qkv, w.seed_qkv, w.dtype)
-d, _ = inputs.draw((1, w.T, w.C), w.sigma_dout, w.seed_dout, w.dtype)
-x = x.astype(np.float64); d = d.astype(np.float64)
+x, _ = inputs.draw((w.B, w.T, 3 * w.C), w.sigma_qkv, w.seed_qkv, w.dtype)
+d, _ = inputs.draw((w.B, w.T, w.C), w.sigma_dout, w.seed_dout, w.dtype)
 heads, t0 = 0, time.perf_counter()
-step_times = []
+fwd_times, bwd_times = [], []
 while heads < max_heads and (time.perf_counter() - t0) < budget:
-    h = heads % w.NH
+    # the batch's (b, h) heads in order, wrapping around after the last
+    b, h = (heads // w.NH) % w.B, heads % w.NH
+    xb = x[b:b + 1].astype(np.float64); db = d[b:b + 1].astype(np.float64)
     s = time.perf_counter()
-    oracle.forward(x, 1, w.T, w.C, w.NH, bool(w.causal), heads=[(0, h)])
-    oracle.backward(d, x, 1, w.T, w.C, w.NH, bool(w.causal), heads=[(0, h)])
-    step_times.append(time.perf_counter() - s)
+    oracle.forward(xb, 1, w.T, w.C, w.NH, bool(w.causal), heads=[(0, h)])
+    m = time.perf_counter()
+    oracle.backward(db, xb, 1, w.T, w.C, w.NH, bool(w.causal), heads=[(0, h)])
+    e = time.perf_counter()
+    fwd_times.append(m - s); bwd_times.append(e - m)
     heads += 1
-print(json.dumps({"heads": heads, "seconds": time.perf_counter() - t0, "step_times": step_times}))
+print(json.dumps({"heads": heads, "seconds": time.perf_counter() - t0, "fwd_times": fwd_times,
+                  "bwd_times": bwd_times}))
 """
 
 
@@ -169,15 +173,31 @@ def run_oracle_child(workload: str, budget_s: float, max_heads: int):
     return json.loads(r.stdout.strip().splitlines()[-1]), cores
 
 
+def _oracle_rates(w, fwd_times, bwd_times):
+    """TFLOP/s of the oracle's forward, backward and forward + backward per head."""
+    f_head = {k: v / (w.B * w.NH) for k, v in flops(w.B, w.T, w.C, w.NH, w.causal).items()}
+    tf, tb = sum(fwd_times), sum(bwd_times)
+    n = len(fwd_times)
+    return {"fwd": n * f_head["fwd"] / tf / 1e12, "bwd": n * f_head["bwd"] / tb / 1e12,
+            "step": n * f_head["step"] / (tf + tb) / 1e12, "fwd_s_per_head": tf / n, "bwd_s_per_head": tb / n}
+
+
+def _sample_text(w, n_heads, seconds, what):
+    return (f"{what}: {n_heads} (b,h) heads of {w.name} taken in order from (0,0) "
+            f"({w.B * w.NH} heads in the batch{', wrapping around' if n_heads > w.B * w.NH else ''}), "
+            f"forward and backward timed apart (the oracle's backward recomputes att itself), "
+            f"float64 numpy oracle, {seconds:.1f} s")
+
+
 def cpu_baseline(workload: str, budget_s: float = 15.0):
     from causal_head_attention_fwd_gb300 import inputs
     w = inputs.WORKLOADS[workload]
     res, cores = run_oracle_child(workload, budget_s, 10_000)
-    f_head = flops(1, w.T, w.C, w.NH, w.causal)["step"] / w.NH
-    value = res["heads"] * f_head / res["seconds"] / 1e12
-    return {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{res['heads']} (b,h) heads of {workload} (of {w.B * w.NH}), fwd+bwd, "
-                      f"float64 numpy oracle, {res['seconds']:.1f} s"}
+    r = _oracle_rates(w, res["fwd_times"], res["bwd_times"])
+    return {"value": r["step"], "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "fwd_tflops": r["fwd"], "bwd_tflops": r["bwd"],
+            "fwd_s_per_head": r["fwd_s_per_head"], "bwd_s_per_head": r["bwd_s_per_head"],
+            "sample": _sample_text(w, res["heads"], res["seconds"], "fwd+bwd")}
 
 
 def run_reference(args):
@@ -188,22 +208,49 @@ def run_reference(args):
     from causal_head_attention_fwd_gb300 import inputs
     w = inputs.WORKLOADS[args.workload]
     res, cores = run_oracle_child(args.workload, 1e9, args.warmup + args.steps)
-    times = res["step_times"][args.warmup:]
-    f_head = flops(1, w.T, w.C, w.NH, w.causal)["step"] / w.NH
-    t = sum(times) / len(times)
-    value = f_head / t / 1e12
+    ft, bt = res["fwd_times"][args.warmup:], res["bwd_times"][args.warmup:]
+    r = _oracle_rates(w, ft, bt)
+    value = r["step"]
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(w),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": (sum(ft) + sum(bt)) / len(ft) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w), "fwd_tflops": r["fwd"], "bwd_tflops": r["bwd"],
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "fwd_tflops": r["fwd"], "bwd_tflops": r["bwd"],
                          "sample": f"one (b,h) head of {w.name} per step (1/{w.B * w.NH} of the batch), "
-                                   "fwd+bwd, float64 numpy oracle"},
+                                   f"heads in order from (0,0); " + _sample_text(w, len(ft), sum(ft) + sum(bt),
+                                                                                   "timed steps")},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def launch_plan(gpus: int, env) -> tuple:
+    """How to honour --gpus N: ("run", None) in this process (N == 1, or N
+    ranks already started by torch.distributed.run with WORLD_SIZE == N),
+    ("spawn", argv) to start N ranks with torch.distributed.run, or
+    ("refuse", reason) when the environment's world size contradicts N."""
+    if gpus < 1:
+        return "refuse", f"--gpus must be >= 1, got {gpus}"
+    ws = env.get("WORLD_SIZE")
+    if ws is not None:
+        if int(ws) != gpus:
+            return "refuse", f"--gpus {gpus} but WORLD_SIZE={ws}: launch {gpus} ranks or pass --gpus {ws}"
+        return "run", None
+    if gpus == 1:
+        return "run", None
+    port = env.get("MASTER_PORT") or str(_free_port())
+    return "spawn", [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={gpus}",
+                     "--master-addr", "127.0.0.1", "--master-port", port]
+
+
+def _free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
 
 
 def config_dict(w):
@@ -472,6 +519,13 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    how, detail = launch_plan(args.gpus, os.environ)
+    if how == "refuse":
+        ap.error(detail)
+    if how == "spawn":
+        # one rank per GPU on this node, each running this same command line
+        return subprocess.call(detail + [str(pathlib.Path(__file__).resolve())] +
+                               list(sys.argv[1:] if argv is None else argv))
     if args.impl == "reference":
         return run_reference(args)
     if args.att:

@@ -41,10 +41,10 @@ def _inputs():
     return [CSRC / s for s in SOURCES] + list(CSRC.glob("*.cuh")) + list(INCLUDE.glob("*.h"))
 
 
-def up_to_date() -> bool:
-    if not LIB.exists():
+def up_to_date(lib: pathlib.Path = LIB) -> bool:
+    if not lib.exists():
         return False
-    t = LIB.stat().st_mtime
+    t = lib.stat().st_mtime
     return all(p.stat().st_mtime <= t for p in _inputs())
 
 
@@ -59,26 +59,34 @@ def _run(cmd, verbose):
     return r
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> pathlib.Path:
-    """Compile and link libattn.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    BUILD.mkdir(exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib: pathlib.Path | None = None,
+          build_dir: pathlib.Path | None = None) -> pathlib.Path:
+    """Compile and link libattn.so; returns its path.
+
+    `extra_flags` (e.g. a -D that changes a compile-time limit), `lib` and
+    `build_dir` build a variant of the library elsewhere, leaving the in-tree
+    libattn.so and its objects untouched."""
+    lib = LIB if lib is None else pathlib.Path(lib)
+    bdir = BUILD if build_dir is None else pathlib.Path(build_dir)
+    if not force and up_to_date(lib):
+        return lib
+    bdir.mkdir(parents=True, exist_ok=True)
+    lib.parent.mkdir(parents=True, exist_ok=True)
     cc = nvcc()
     jobs = []
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         for s in SOURCES:
-            obj = BUILD / (pathlib.Path(s).stem + ".o")
+            obj = bdir / (pathlib.Path(s).stem + ".o")
             cmd = [cc, *NVCC_FLAGS, *extra_flags, "-c", str(CSRC / s), "-o", str(obj)]
             jobs.append((obj, ex.submit(_run, cmd, verbose)))
         objs = []
         for obj, fut in jobs:
             fut.result()
             objs.append(str(obj))
-    tmp = LIB.with_suffix(".so.tmp")
+    tmp = lib.with_suffix(".so.tmp")
     _run([cc, *ARCH, "-shared", "-o", str(tmp), *objs], verbose)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 def main(argv=None):

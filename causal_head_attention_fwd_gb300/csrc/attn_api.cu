@@ -48,19 +48,48 @@ cudaError_t launch_decode(const CUtensorMap& map_qkv, const void* qkv, void* out
 static __device__ int g_error_word = 0;
 
 static constexpr int kMaxDevices = 64;
-static int* g_error_addr[kMaxDevices] = {nullptr};
 static std::mutex g_mu;
+
+// Id of the calling thread's current CUDA context, unique for the life of the
+// process (a context made after cudaDeviceReset gets a new one, even if its
+// handle value is reused). False when no context is current or the driver
+// entry point is unavailable.
+bool current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetId_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  return fn && fn(nullptr, id) == CUDA_SUCCESS;
+}
+
+// The device address of a __device__ symbol is a property of the module loaded
+// into one context: it is looked up once per device and looked up again when
+// that device's context has changed (after cudaDeviceReset the module is
+// loaded anew and the symbol may move).
+struct SymbolAddr {
+  unsigned long long ctx = 0;
+  int* addr = nullptr;
+};
+static SymbolAddr g_error_addr[kMaxDevices];
 
 int* device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_error_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-    g_error_addr[dev] = static_cast<int*>(p);
+  unsigned long long id = 0;
+  SymbolAddr& c = g_error_addr[dev];
+  if (!c.addr || !current_context_id(&id) || id != c.ctx) {
+    void* p = nullptr;   // the lookup makes the device's primary context current if none is
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess || !current_context_id(&id)) return nullptr;
+    c.addr = static_cast<int*>(p);
+    c.ctx = id;
   }
-  return g_error_addr[dev];
+  return c.addr;
 }
 
 static int g_sm_count[kMaxDevices] = {0};

@@ -13,9 +13,12 @@
 // (32 MiB). Every GPU that loads the library holds it until the process exits.
 // In host code its name is only a host-side stand-in, never a device address,
 // so the first call on each device looks up the real address with
-// cudaGetSymbolAddress (with that device current) and caches it; make that
-// first call before any stream capture. Nothing here calls cudaMalloc,
-// cudaFree or an allocating library routine.
+// cudaGetSymbolAddress (with that device current) and caches it together with
+// the id of the device's context; a later call in a different context (after
+// cudaDeviceReset, say, when the module is loaded anew and the array may move)
+// looks it up again. Make the first call on a device before any stream
+// capture. Nothing here calls cudaMalloc, cudaFree or an allocating library
+// routine.
 //
 // All calls share the one array and it keeps the previous call's contents: the
 // backward's pre-pass zeroes the dq accumulator and rewrites D on every call,
@@ -29,6 +32,10 @@
 
 #include "../../include/attn.h"
 
+namespace attn {
+bool current_context_id(unsigned long long* id);   // attn_api.cu
+}
+
 namespace {
 
 constexpr size_t kScratchBytes = ATTN_NOALLOC_SCRATCH_BYTES;
@@ -37,20 +44,29 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+struct Cached {
+  unsigned long long ctx = 0;   // id of the context the address belongs to
+  void* addr = nullptr;
+};
+Cached g_scratch[kMaxDevices];
 
-// Device address of the scratch array on the current device (looked up once).
+// Device address of the scratch array in the current device's context (looked
+// up once per context).
 attn_status_t scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_setup_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
+  Cached& c = g_scratch[dev];
+  unsigned long long id = 0;
+  if (!c.addr || !attn::current_context_id(&id) || id != c.ctx) {
+    void* p = nullptr;   // the lookup makes the device's primary context current if none is
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    if (!attn::current_context_id(&id)) return ATTN_ERR_CUDA;
+    c.addr = p;
+    c.ctx = id;
   }
-  *out = g_scratch_addr[dev];
+  *out = c.addr;
   return ATTN_OK;
 }
 

@@ -345,13 +345,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_p[wg]);
       }
-      if (!ok) break;
       // -------------------------------------------------------- epilogue of this item
+      // A warp whose wait gave up left the key loop early, but it still comes
+      // here: failures are combined over the warpgroup at the barrier below, so
+      // the four warps always leave together and none is left at a barrier.
       uint8_t* stage = smem + L::Q_OFF + (2 * qb + wg) * G::TILE_BYTES;   // this Q tile is dead now
       if (n > 0) {
-        // failures are combined over the warpgroup at the barrier, so a bounded
-        // wait that gave up never leaves a thread stuck at the barrier
-        const bool fail = !mbar_wait(&bar_pv[wg], (gs + n - 1) & 1, &abort_sh, gerr);
+        const bool fail = !ok || !mbar_wait(&bar_pv[wg], (gs + n - 1) & 1, &abort_sh, gerr);
         tc_fence_after();
         const float inv_l = 1.f / l_run;
 #pragma unroll

@@ -375,10 +375,12 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_p[wg]);
       }
-      if (!ok) break;
       // ---------------------------------------------------------- epilogue of this item
+      // A warp whose wait gave up left the key loop early, but it still comes
+      // here: failures are combined over the warpgroup at the barrier below, so
+      // the four warps always leave together and none is left at a barrier.
       if (n > 0) {
-        const bool fail = !mbar_wait(&bar_pv[wg], (gs + n - 1) & 1, &abort_sh, gerr);
+        const bool fail = !ok || !mbar_wait(&bar_pv[wg], (gs + n - 1) & 1, &abort_sh, gerr);
         tc_fence_after();
         const float f = dv / l_run;
         // the previous item's store of this staging tile must have read it

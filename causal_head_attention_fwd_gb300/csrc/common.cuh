@@ -41,6 +41,9 @@ struct Problem {
 // attn_status_t code written by a kernel whose bounded wait gave up).
 int* device_error_word();
 
+// Process-unique id of the current CUDA context (false if none is current).
+bool current_context_id(unsigned long long* id);
+
 // Number of SMs of the current device (cached; persistent grids are sized by it).
 int device_sm_count();
 

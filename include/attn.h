@@ -200,9 +200,14 @@ attn_status_t attn_last_device_error(void* stream);
  * device memory, ATTN_NOALLOC_SCRATCH_BYTES per GPU that loads the library,
  * held until the process exits. This call allocates nothing.
  *   - Returns ATTN_ERR_WORKSPACE when attn_bwd_workspace_size(...) exceeds
- *     ATTN_NOALLOC_SCRATCH_BYTES (roughly B*T*C*4 + B*NH*T*4 bytes must fit).
- *   - The first call on each device looks up the array's device address;
- *     make that first call before any stream capture.
+ *     ATTN_NOALLOC_SCRATCH_BYTES. With r256(x) = x rounded up to a multiple
+ *     of 256: bf16 needs r256(B*NH*T*4) + B*T*C*4 bytes (D and the fp32 dq
+ *     accumulator), fp32 needs r256(B*NH*T*4) (D only: its dq goes straight
+ *     into dqkv).
+ *   - The first call on each device looks up the array's device address in
+ *     that device's current context; make that first call before any stream
+ *     capture. A call made in another context of the device (after
+ *     cudaDeviceReset, for example) looks the address up again.
  *   - Every call shares the one array (the previous call's contents remain,
  *     and each call re-initialises what must start at zero). Calls whose GPU
  *     work overlaps, on different streams or from different host threads,
@@ -247,12 +252,17 @@ attn_status_t attn_selftest_wait_timeout(unsigned int limit_us, void* stream);
  * benchmark timing loop). While enabled, every kernel the library launches is
  * bracketed by two CUDA events recorded on its stream; attn_profile_read
  * synchronises those events and returns the accumulated device time (ms) and
- * launch count of one kernel since the last reset. Kernel ids:
- *   0 forward, 1 backward pre-pass (D, zero dq accumulator),
- *   2 backward main kernel, 3 backward dq conversion, 4 linear layer.
+ * launch count of one kernel since the last reset. Kernel ids are the
+ * ATTN_PROFILE_* values below (the fp32 path's four kernels share the first
+ * four slots: forward, D pre-pass, dK/dV kernel, dQ kernel).
  * Enabling adds two event records per launch; leave it off for timing runs.
  * Not thread-safe with concurrent attn_fwd/attn_bwd calls from other threads.
  */
+#define ATTN_PROFILE_FWD 0        /* forward */
+#define ATTN_PROFILE_BWD_PRE 1    /* backward pre-pass: D */
+#define ATTN_PROFILE_BWD_MAIN 2   /* backward main kernel */
+#define ATTN_PROFILE_BWD_DQ 3     /* backward dq pass */
+#define ATTN_PROFILE_LINEAR 4     /* linear layer (c_attn / c_proj) */
 #define ATTN_PROFILE_NUM_KERNELS 5
 attn_status_t attn_profile_enable(int enable);
 attn_status_t attn_profile_reset(void);

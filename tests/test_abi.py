@@ -44,6 +44,36 @@ def test_library_exports_every_declared_symbol(api):
     assert set(api.EXPORTED) <= set(_declared())
 
 
+def _header_constants():
+    """Enumerators and #define values of include/attn.h, by name."""
+    text = (ROOT / "include" / "attn.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    vals = {}
+    for body in re.findall(r"typedef\s+enum\s*\{(.*?)\}", text, flags=re.S):
+        for name, v in re.findall(r"\b(ATTN_[A-Z0-9_]+)\s*=\s*(\d+)", body):
+            vals[name] = int(v)
+    for name, expr in re.findall(r"#define[ \t]+(ATTN_[A-Z0-9_]+)[ \t]+([^\n]+)", text):
+        m = re.fullmatch(r"\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", expr.strip())
+        vals[name] = int(m.group(1)) << int(m.group(2)) if m else int(expr.strip())
+    return vals
+
+
+def test_python_constants_match_the_header(api):
+    """The binding mirrors the header's constants by hand; they must agree."""
+    h = _header_constants()
+    for name in ("ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
+                 "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_F32", "ATTN_BF16"):
+        assert getattr(api, name) == h[name], name
+    assert api.NOALLOC_SCRATCH_BYTES == h["ATTN_NOALLOC_SCRATCH_BYTES"]
+    ids = {"K_FWD": "ATTN_PROFILE_FWD", "K_BWD_PRE": "ATTN_PROFILE_BWD_PRE", "K_BWD_MAIN": "ATTN_PROFILE_BWD_MAIN",
+           "K_BWD_DQ": "ATTN_PROFILE_BWD_DQ", "K_LINEAR": "ATTN_PROFILE_LINEAR"}
+    for py, c in ids.items():
+        assert getattr(api, py) == h[c], py
+    assert len(ids) == h["ATTN_PROFILE_NUM_KERNELS"]
+    # the binding covers every entry point the header declares
+    assert set(api.EXPORTED) == set(_declared())
+
+
 def test_status_strings(api):
     for s in range(7):
         assert api.attn_status_string(s).startswith("ATTN_")

@@ -26,6 +26,33 @@ def test_reference_arm_line():
     assert d["config"]["workload"].startswith("gpt2s_bf16")
 
 
+def test_reference_arm_times_fwd_and_bwd_apart():
+    d = _line(["--impl", "reference", "--steps", "2", "--warmup", "3"])
+    cb = d["cpu_baseline"]
+    assert cb["fwd_tflops"] > 0 and cb["bwd_tflops"] > 0
+    # fwd+bwd rate lies between the two separate rates
+    assert min(cb["fwd_tflops"], cb["bwd_tflops"]) <= d["value"] <= max(cb["fwd_tflops"], cb["bwd_tflops"])
+    assert "heads in order" in cb["sample"]
+
+
+def test_gpus_flag_launch_plan():
+    """--gpus N starts N ranks itself, runs as it is under torch.distributed.run
+    with a matching WORLD_SIZE, and refuses a mismatched one."""
+    assert bench.launch_plan(1, {}) == ("run", None)
+    how, argv = bench.launch_plan(4, {})
+    assert how == "spawn" and "--nproc-per-node=4" in argv and "127.0.0.1" in argv
+    assert bench.launch_plan(4, {"WORLD_SIZE": "4"}) == ("run", None)
+    how, why = bench.launch_plan(8, {"WORLD_SIZE": "2"})
+    assert how == "refuse" and "WORLD_SIZE=2" in why
+    assert bench.launch_plan(0, {})[0] == "refuse"
+
+
+def test_mismatched_world_size_is_refused(monkeypatch):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    with pytest.raises(SystemExit):
+        bench.main(["--gpus", "4", "--steps", "1", "--warmup", "3"])
+
+
 def test_warmup_below_three_is_refused():
     with pytest.raises(SystemExit):
         bench.main(["--steps", "1", "--warmup", "2"])
