@@ -24,26 +24,34 @@
 //   3. attn_bwd_dq_out: dq accumulator -> bf16 into dqkv[:, :, 0:C].
 //
 // Main kernel: 16 warps.
-//   warps 0-3   softmax warpgroup A: query columns [0, 64) of S^T/dP^T, thread = key row
-//   warps 4-7   softmax warpgroup B: query columns [64, 128)
+//   warps 0-3   P/dS warpgroup A: keys [0, 64) of the tile, thread = query row
+//   warps 4-7   P/dS warpgroup B: keys [64, 128)
 //   warps 8-11  dQ warpgroup: thread = query row; TMEM -> smem -> TMA reduce-add;
 //               after each item the dK/dV epilogue (thread = key row)
-//   warp  12    loader: K, V per item; Q, dO, lse, D per query tile (3-stage ring)
-//   warp  13    MMA issuer; warps 14-15 idle
-// The softmax warpgroups copy S^T/dP^T of step g into registers and release
-// them at once, so the tensor core computes S^T/dP^T of step g+1 while P/dS of
-// step g are formed. MMA order: S(g), dP(g), dK(g-1), dQ(g-1), dV(g-1): the dS^T
-// tile is released before dV runs, so the next one is written meanwhile.
-// TMEM columns: S^T [0,128) dP^T [128,256) P^T [256,320) dV [320,384)
-//               dK [384,448) dQ [448,512)
+//   warp  12    loader: K per item (double-buffered), Q and dO per query tile
+//               (3-stage ring)
+//   warp  13    MMA issuer
+//   warp  14    loader of V (one buffer, refilled once the item's last dP is done)
+//   warp  15    idle
+// With the query row as the thread (the TMEM lane of S = Q K^T and dP = dO V^T),
+// the row statistics lse_t and D_t are two registers per thread, read from
+// global memory one step ahead: the P/dS phase reads no shared memory. P and dS
+// go to shared memory as [key block][query][64 keys] tiles, the MN-major A
+// operands of dV += P^T dO and dK += dS^T Q; dS also goes to TMEM as the A
+// operand of dQ = dS K.
+// The P/dS warpgroups copy S/dP of step g into registers and release them at
+// once, so the tensor core computes S/dP of step g+1 while P/dS of step g are
+// formed. MMA order: S(g), dP(g), dK(g-1), dQ(g-1), dV(g-1).
+// TMEM columns: S [0,128) dP [128,256) dV [256,320) dK [320,384) dQ [384,448)
+//               dS [448,512) (bf16 pairs)
 #include "common.cuh"
 
 namespace attn {
 
 constexpr int BWD_STAGES = 3;
 constexpr int BWD_THREADS = 512;
-constexpr uint32_t TB_S = 0, TB_DP = 128, TB_P = 256, TB_DV = 320, TB_DK = 384, TB_DQ = 448;
-// register split: 2 softmax warpgroups up, the other 2 warpgroups down.
+constexpr uint32_t TB_S = 0, TB_DP = 128, TB_DV = 256, TB_DK = 320, TB_DQ = 384, TB_DS = 448;
+// register split: 2 P/dS warpgroups up, the other 2 warpgroups down.
 // pool = 512 threads x 128 registers = 65536 = 256 x 160 + 256 x 96.
 constexpr uint32_t REG_SOFTMAX = 160, REG_OTHER = 96;
 static_assert(256 * REG_SOFTMAX + 256 * REG_OTHER <= 512 * 128, "register split exceeds the pool");
@@ -52,17 +60,18 @@ template <int HS>
 struct BwdSmem {
   static constexpr int TILE = TileGeom<HS>::TILE_BYTES;
   static constexpr int K_OFF = 0;                              // 2 buffers
-  static constexpr int V_OFF = K_OFF + 2 * TILE;               // 2 buffers
-  static constexpr int Q_OFF = V_OFF + 2 * TILE;               // BWD_STAGES tiles
+  static constexpr int V_OFF = K_OFF + 2 * TILE;               // 1 buffer
+  static constexpr int Q_OFF = V_OFF + TILE;                   // BWD_STAGES tiles
   static constexpr int DO_OFF = Q_OFF + BWD_STAGES * TILE;     // BWD_STAGES tiles
-  static constexpr int DS_OFF = DO_OFF + BWD_STAGES * TILE;    // dS^T: 2 blocks of [128 keys][64 q] bf16
-  static constexpr int DS_BYTES = 2 * 128 * 128;
-  static constexpr int DQ_OFF = DS_OFF + DS_BYTES;             // dQ fp32 [128 q][32] SW128 block; dK/dV staging
+  static constexpr int P_OFF = DO_OFF + BWD_STAGES * TILE;     // P: [2 key blocks][128 q][64 keys] bf16, SW128
+  static constexpr int PT_BYTES = 2 * 128 * 128;
+  static constexpr int DS_OFF = P_OFF + PT_BYTES;              // dS, same layout
+  static constexpr int DQ_OFF = DS_OFF + PT_BYTES;             // dQ fp32 [128 q][32] SW128 block; dK/dV staging
   static constexpr int DQ_BYTES = 128 * 128;
-  static constexpr int ROWST_OFF = DQ_OFF + DQ_BYTES;          // per stage: -lse*log2e [128], D [128]
-  static constexpr int BYTES = ROWST_OFF + BWD_STAGES * 2 * 128 * 4;
+  static constexpr int BYTES = DQ_OFF + DQ_BYTES;
   static constexpr int ALLOC = BYTES + 1024;
   static_assert(TILE <= DQ_BYTES, "dK/dV staging must fit in the dQ staging area");
+  static_assert(P_OFF % 1024 == 0, "P/dS tiles must start on a 128-byte-swizzle atom");
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -160,39 +169,31 @@ __global__ void attn_bwd_dq_out(const float4* __restrict__ dq_acc, uint4* __rest
 }
 
 // ----------------------------------------------------------------------------
-// P^T and dS^T of 64 query columns for one key row (packed fp32 pair math):
-//   P  = exp2(s*c - lse*log2 e),   dS = P * (dP - D)
-// rs holds -lse*log2(e) for the 128 queries of the tile, then D. With MASK,
-// queries before the key (causal diagonal tile) and keys past T give 0.
+// P and dS of one query row over 64 keys (packed fp32 pair math):
+//   P = exp2(s*c - lse*log2 e),   dS = P * (dP - D)
+// nl = -lse*log2(e) of the row (-inf for rows past T, so P = 0 there), Dq its
+// D. With MASK, keys at or past `lim` (causal diagonal, keys past T) give 0.
 // ----------------------------------------------------------------------------
 template <bool MASK>
-__device__ __forceinline__ void bwd_p_ds(const uint32_t (&sv)[2][32], const uint32_t (&dpv)[2][32],
-                                         const float* rs, float c, int q0, int r, bool diag, bool key_ok,
-                                         uint32_t (&pk)[32], uint32_t (&dk)[32]) {
-  const float2 c2 = make_float2(c, c);
+__device__ __forceinline__ void bwd_p_ds(const uint32_t (&sv)[2][32], const uint32_t (&dpv)[2][32], float nl,
+                                         float Dq, float c, int lim, uint32_t (&pk)[32], uint32_t (&dk)[32]) {
+  const float2 c2 = make_float2(c, c), nl2 = make_float2(nl, nl), d2 = make_float2(Dq, Dq);
 #pragma unroll
   for (int cq = 0; cq < 2; ++cq) {
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      const float4 l4 = *reinterpret_cast<const float4*>(rs + cq * 32 + i);
-      const float4 d4 = *reinterpret_cast<const float4*>(rs + 128 + cq * 32 + i);
-#pragma unroll
-      for (int u = 0; u < 4; u += 2) {
-        const float2 nl = u == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
-        const float2 dd = u == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
-        const float2 s2 = make_float2(__uint_as_float(sv[cq][i + u]), __uint_as_float(sv[cq][i + u + 1]));
-        const float2 dp2 = make_float2(__uint_as_float(dpv[cq][i + u]), __uint_as_float(dpv[cq][i + u + 1]));
-        const float2 x = fma2(s2, c2, nl);
-        float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        if (MASK) {
-          const int qq = q0 + cq * 32 + i + u;       // query index in the tile
-          if (!key_ok || (diag && qq < r)) e.x = 0.f;
-          if (!key_ok || (diag && qq + 1 < r)) e.y = 0.f;
-        }
-        const float2 ds = mul2(e, sub2(dp2, dd));
-        pk[cq * 16 + (i + u) / 2] = pack_bf16x2(e.x, e.y);
-        dk[cq * 16 + (i + u) / 2] = pack_bf16x2(ds.x, ds.y);
+    for (int i = 0; i < 32; i += 2) {
+      const float2 s2 = make_float2(__uint_as_float(sv[cq][i]), __uint_as_float(sv[cq][i + 1]));
+      const float2 dp2 = make_float2(__uint_as_float(dpv[cq][i]), __uint_as_float(dpv[cq][i + 1]));
+      const float2 x = fma2(s2, c2, nl2);
+      float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+      if (MASK) {
+        const int col = cq * 32 + i;             // key index in this 64-key half
+        if (col >= lim) e.x = 0.f;
+        if (col + 1 >= lim) e.y = 0.f;
       }
+      const float2 ds = mul2(e, sub2(dp2, d2));
+      pk[cq * 16 + i / 2] = pack_bf16x2(e.x, e.y);
+      dk[cq * 16 + i / 2] = pack_bf16x2(ds.x, ds.y);
     }
   }
 }
@@ -210,7 +211,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  __shared__ uint64_t bar_kv_full[2], bar_kv_empty[2], bar_q_full[BWD_STAGES], bar_q_empty[BWD_STAGES];
+  __shared__ uint64_t bar_k_full[2], bar_k_empty[2], bar_v_full, bar_v_empty;
+  __shared__ uint64_t bar_q_full[BWD_STAGES], bar_q_empty[BWD_STAGES];
   __shared__ uint64_t bar_sdp_full, bar_sdp_free, bar_pds_full, bar_ds_free, bar_p_free, bar_dq_full, bar_dq_free,
       bar_done, bar_epi_free;
   __shared__ uint32_t tmem_base_sh;
@@ -231,18 +233,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
   if (threadIdx.x == 0) {
     abort_sh = 0;
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_kv_full[s], 1);
-      mbar_init(&bar_kv_empty[s], 1);
+      mbar_init(&bar_k_full[s], 1);
+      mbar_init(&bar_k_empty[s], 1);
     }
+    mbar_init(&bar_v_full, 1);
+    mbar_init(&bar_v_empty, 1);
     for (int s = 0; s < BWD_STAGES; ++s) {
       mbar_init(&bar_q_full[s], 1);
       mbar_init(&bar_q_empty[s], 1);
     }
     mbar_init(&bar_sdp_full, 1);
-    mbar_init(&bar_sdp_free, 8);                 // one arrival per softmax warp
+    mbar_init(&bar_sdp_free, 8);                 // one arrival per P/dS warp
     mbar_init(&bar_pds_full, 8);
-    mbar_init(&bar_ds_free, 1);                  // dK, dQ of the step read the dS^T tile
-    mbar_init(&bar_p_free, 1);                   // dV of the step read P^T
+    mbar_init(&bar_ds_free, 1);                  // dK and dQ of the step read dS (smem and TMEM)
+    mbar_init(&bar_p_free, 1);                   // dV of the step read P
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_free, 4);                  // one arrival per dQ warp
     mbar_init(&bar_done, 1);
@@ -263,119 +267,92 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
   if (warp >= 8) {
     setmaxnreg_dec<REG_OTHER>();
     if (warp == 12) {
-      // ------------------------------------------------------------ loader
+      // ------------------------------------------------------------ loader: K, Q, dO
       if (lane == 0) {
         tma_prefetch_desc(&map_qkv);
         tma_prefetch_desc(&map_dout);
-      }
-      // per query tile: -lse*log2(e) and D of its 128 rows, loaded into registers
-      // one step ahead so their latency hides behind the ring wait
-      const float nlog2e = -1.4426950408889634f;
-      float lv[4], dv[4];
-      auto load_rows = [&](int bh, int qi) {
-        const size_t rowbase = (size_t)bh * T;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int q = qi * BM + lane + 32 * k;
-          // rows past T: -lse2 = -inf makes P = 0 there, D = 0
-          lv[k] = q < T ? __ldg(p.lse + rowbase + q) * nlog2e : -INFINITY;
-          dv[k] = q < T ? __ldg(p.D + rowbase + q) : 0.f;
-        }
-      };
-      bool ok = true;
-      int g = 0;
-      if (n_items_cta > 0) {
-        const BwdItem f = bwd_decode<CAUSAL>(bwd_item(0), p);
-        load_rows(f.bh, f.i0);
-      }
-      for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-        const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
-        const int kb = ic & 1;
-        if (ic >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&bar_kv_empty[kb], ((ic >> 1) - 1) & 1, &abort_sh, gerr));
-        if (!ok) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_kv_full[kb], 2 * G::TILE_BYTES);
-          tma_load_3d(smem + L::K_OFF + kb * G::TILE_BYTES, &map_qkv, &bar_kv_full[kb], p.C + w.h * HS, w.kv * BN, w.b);
-          tma_load_3d(smem + L::V_OFF + kb * G::TILE_BYTES, &map_qkv, &bar_kv_full[kb], 2 * p.C + w.h * HS, w.kv * BN, w.b);
-        }
-        for (int it = 0; it < w.n_it; ++it, ++g) {
-          const int st = g % BWD_STAGES;
-          const int qi = w.i0 + it;
-          if (g >= BWD_STAGES)
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar_q_empty[st], ((g / BWD_STAGES) - 1) & 1, &abort_sh, gerr));
-          if (!ok) break;
-          if (lane == 0) {
-            mbar_expect_tx(&bar_q_full[st], 2 * G::TILE_BYTES);
+        bool ok = true;
+        int g = 0;
+        for (int ic = 0; ok && ic < n_items_cta; ++ic) {
+          const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
+          const int kb = ic & 1;
+          if (ic >= 2 && !(ok = mbar_wait(&bar_k_empty[kb], ((ic >> 1) - 1) & 1, &abort_sh, gerr))) break;
+          mbar_arrive_expect_tx(&bar_k_full[kb], G::TILE_BYTES);
+          tma_load_3d(smem + L::K_OFF + kb * G::TILE_BYTES, &map_qkv, &bar_k_full[kb], p.C + w.h * HS, w.kv * BN, w.b);
+          for (int it = 0; it < w.n_it; ++it, ++g) {
+            const int st = g % BWD_STAGES;
+            const int qi = w.i0 + it;
+            if (g >= BWD_STAGES &&
+                !(ok = mbar_wait(&bar_q_empty[st], ((g / BWD_STAGES) - 1) & 1, &abort_sh, gerr)))
+              break;
+            mbar_arrive_expect_tx(&bar_q_full[st], 2 * G::TILE_BYTES);
             tma_load_3d(smem + L::Q_OFF + st * G::TILE_BYTES, &map_qkv, &bar_q_full[st], w.h * HS, qi * BM, w.b);
             tma_load_3d(smem + L::DO_OFF + st * G::TILE_BYTES, &map_dout, &bar_q_full[st], w.h * HS, qi * BM, w.b);
           }
-          float* rs = reinterpret_cast<float*>(smem + L::ROWST_OFF) + st * 256;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            rs[lane + 32 * k] = lv[k];
-            rs[128 + lane + 32 * k] = dv[k];
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar_q_full[st]);
-          // prefetch the rows of the next step (this item or the next one)
-          if (it + 1 < w.n_it) {
-            load_rows(w.bh, qi + 1);
-          } else if (ic + 1 < n_items_cta) {
-            const BwdItem nx = bwd_decode<CAUSAL>(bwd_item(ic + 1), p);
-            load_rows(nx.bh, nx.i0);
-          }
+        }
+      }
+    } else if (warp == 14) {
+      // ------------------------------------------------------------ loader: V
+      if (lane == 0) {
+        for (int ic = 0; ic < n_items_cta; ++ic) {
+          const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
+          // the previous item's dP steps must be done with the buffer
+          if (ic >= 1 && !mbar_wait(&bar_v_empty, (ic - 1) & 1, &abort_sh, gerr)) break;
+          mbar_arrive_expect_tx(&bar_v_full, G::TILE_BYTES);
+          tma_load_3d(smem + L::V_OFF, &map_qkv, &bar_v_full, 2 * p.C + w.h * HS, w.kv * BN, w.b);
         }
       }
     } else if (warp == 13) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
-        constexpr uint32_t id_sq = make_idesc_bf16(BN, BM, false, false);   // [keys x q], K = HS
-        constexpr uint32_t id_kv = make_idesc_bf16(BN, HS, false, true);    // [keys x HS], K = q, B MN-major
-        constexpr uint32_t id_dq = make_idesc_bf16(BM, HS, true, true);     // [q x HS], K = keys, A,B MN-major
+        constexpr uint32_t id_s = make_idesc_bf16(BM, BN, false, false);     // [q x keys], K = HS, both K-major
+        constexpr uint32_t id_acc = make_idesc_bf16(BN, HS, true, true);     // [keys x HS], K = q: A, B MN-major
+        constexpr uint32_t id_dq = make_idesc_bf16(BM, HS, false, true);     // [q x HS], K = keys: A TMEM, B MN-major
         const uint64_t dK0 = make_sdesc(smem_u32(smem + L::K_OFF), 16, G::ATOM_BYTES, G::SWZ);
         const uint64_t dV0 = make_sdesc(smem_u32(smem + L::V_OFF), 16, G::ATOM_BYTES, G::SWZ);
         const uint64_t dQ0 = make_sdesc(smem_u32(smem + L::Q_OFF), 16, G::ATOM_BYTES, G::SWZ);
         const uint64_t dO0 = make_sdesc(smem_u32(smem + L::DO_OFF), 16, G::ATOM_BYTES, G::SWZ);
-        const uint64_t dSk = make_sdesc(smem_u32(smem + L::DS_OFF), 16, 1024, SWZ_128B);      // dS^T, K-major
-        const uint64_t dSm = make_sdesc(smem_u32(smem + L::DS_OFF), 16384, 1024, SWZ_128B);   // dS, MN-major
-        // the step whose dV/dK/dQ are still to be issued
+        // P^T, dS^T as MN-major A operands: M = keys, two 64-key atoms LBO = 16 KB
+        // apart, K = queries in rows of 128 bytes (SBO = 8 rows)
+        const uint64_t dPm = make_sdesc(smem_u32(smem + L::P_OFF), 16384, 1024, SWZ_128B);
+        const uint64_t dSm = make_sdesc(smem_u32(smem + L::DS_OFF), 16384, 1024, SWZ_128B);
+        // the step whose dK/dQ/dV are still to be issued
         struct Pend { int g, st, kb, ic; bool first, last; };
         bool ok = true;
-        // dV, dK, dQ of step f
         auto finish = [&](const Pend& f) -> bool {
           const uint64_t qd = desc_add(dQ0, f.st * G::TILE_BYTES), od = desc_add(dO0, f.st * G::TILE_BYTES);
           if (!mbar_wait(&bar_pds_full, f.g & 1, &abort_sh, gerr)) return false;
           // dK/dV of the previous item must have been read out by its epilogue
           if (f.first && f.ic > 0 && !mbar_wait(&bar_epi_free, (f.ic - 1) & 1, &abort_sh, gerr)) return false;
           tc_fence_after();
-          // dK += dS^T Q  (A = dS^T K-major: 2 blocks of 64 queries, B = Q MN-major)
+          // dK += dS^T Q  (K = 128 queries: 16 rows of the dS tile per instruction)
 #pragma unroll
           for (int k = 0; k < BM / 16; ++k)
-            mma_ss(tmem + TB_DK, desc_add(dSk, (k / 4) * 16384 + (k % 4) * 32),
-                   desc_add(qd, k * 16 * G::ROW_BYTES), id_kv, (!f.first || k > 0) ? 1u : 0u);
+            mma_ss(tmem + TB_DK, desc_add(dSm, k * 16 * 128), desc_add(qd, k * 16 * G::ROW_BYTES), id_acc,
+                   (!f.first || k > 0) ? 1u : 0u);
           if (f.g > 0) {
             if (!mbar_wait(&bar_dq_free, (f.g - 1) & 1, &abort_sh, gerr)) return false;
             tc_fence_after();
           }
-          // dQ = dS K  (A = dS: MN-major view of the dS^T tile, B = K MN-major; K-dim = 128 keys)
+          // dQ = dS K  (A = dS from TMEM, K = 128 keys = 64 columns of bf16 pairs)
           const uint64_t kd = desc_add(dK0, f.kb * G::TILE_BYTES);
 #pragma unroll
           for (int k = 0; k < BN / 16; ++k)
-            mma_ss(tmem + TB_DQ, desc_add(dSm, k * 16 * 128), desc_add(kd, k * 16 * G::ROW_BYTES), id_dq, k > 0);
+            mma_ts(tmem + TB_DQ, tmem + TB_DS + k * 8, desc_add(kd, k * 16 * G::ROW_BYTES), id_dq, k > 0);
           mma_commit(&bar_dq_full);
-          // the dS^T tile is free once dK and dQ are done: the softmax warps write
-          // the next one while dV still runs (only commits that someone waits for)
+          // dS (smem and TMEM) is free once dK and dQ are done: the next one is
+          // written while dV still runs (only commits that someone waits for)
           if (f.g + 1 < total_g) mma_commit(&bar_ds_free);
-          // dV += P^T dO  (A = P^T in TMEM, B = dO MN-major; K = 128 queries)
+          // dV += P^T dO
 #pragma unroll
           for (int k = 0; k < BM / 16; ++k)
-            mma_ts(tmem + TB_DV, tmem + TB_P + k * 8, desc_add(od, k * 16 * G::ROW_BYTES), id_kv,
+            mma_ss(tmem + TB_DV, desc_add(dPm, k * 16 * 128), desc_add(od, k * 16 * G::ROW_BYTES), id_acc,
                    (!f.first || k > 0) ? 1u : 0u);
           if (f.g + 1 < total_g) mma_commit(&bar_p_free);
           if (f.g + BWD_STAGES < total_g) mma_commit(&bar_q_empty[f.st]);
           if (f.last) {
             mma_commit(&bar_done);                           // dK/dV of item f.ic final
-            if (f.ic + 2 < n_items_cta) mma_commit(&bar_kv_empty[f.kb]);
+            if (f.ic + 2 < n_items_cta) mma_commit(&bar_k_empty[f.kb]);
           }
           return true;
         };
@@ -385,22 +362,25 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
         for (int ic = 0; ok && ic < n_items_cta; ++ic) {
           const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
           const int kb = ic & 1;
-          if (!(ok = mbar_wait(&bar_kv_full[kb], (ic >> 1) & 1, &abort_sh, gerr))) break;
-          const uint64_t kd = desc_add(dK0, kb * G::TILE_BYTES), vd = desc_add(dV0, kb * G::TILE_BYTES);
+          if (!(ok = mbar_wait(&bar_k_full[kb], (ic >> 1) & 1, &abort_sh, gerr))) break;
+          if (!(ok = mbar_wait(&bar_v_full, ic & 1, &abort_sh, gerr))) break;
+          const uint64_t kd = desc_add(dK0, kb * G::TILE_BYTES);
           for (int it = 0; ok && it < w.n_it; ++it, ++g) {
             const int st = g % BWD_STAGES;
             if (!(ok = mbar_wait(&bar_q_full[st], (g / BWD_STAGES) & 1, &abort_sh, gerr))) break;
             if (g > 0 && !(ok = mbar_wait(&bar_sdp_free, (g - 1) & 1, &abort_sh, gerr))) break;
             tc_fence_after();
             const uint64_t qd = desc_add(dQ0, st * G::TILE_BYTES), od = desc_add(dO0, st * G::TILE_BYTES);
-            // S^T = K Q^T ; dP^T = V dO^T   (K-dim = HS)
+            // S = Q K^T ; dP = dO V^T   (K-dim = HS, both operands K-major)
 #pragma unroll
             for (int k = 0; k < HS / 16; ++k)
-              mma_ss(tmem + TB_S, desc_add(kd, k * 32), desc_add(qd, k * 32), id_sq, k > 0);
+              mma_ss(tmem + TB_S, desc_add(qd, k * 32), desc_add(kd, k * 32), id_s, k > 0);
 #pragma unroll
             for (int k = 0; k < HS / 16; ++k)
-              mma_ss(tmem + TB_DP, desc_add(vd, k * 32), desc_add(od, k * 32), id_sq, k > 0);
+              mma_ss(tmem + TB_DP, desc_add(od, k * 32), desc_add(dV0, k * 32), id_s, k > 0);
             mma_commit(&bar_sdp_full);
+            // V is free for the next item once this item's last dP is done
+            if (it == w.n_it - 1 && ic + 1 < n_items_cta) mma_commit(&bar_v_empty);
             if (have_pend) ok = finish(pend);
             pend = Pend{g, st, kb, ic, it == 0, it == w.n_it - 1};
             have_pend = true;
@@ -502,23 +482,41 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
     }
   } else {
     setmaxnreg_inc<REG_SOFTMAX>();
-    // ------------------------------------------------------------ softmax warpgroups
-    const int half = warp >> 2;                    // query columns [64*half, 64*half+64)
-    const int r = ((warp & 3) << 5) + lane;        // key row in the tile = TMEM lane
+    // ------------------------------------------------------------ P/dS warpgroups
+    const int half = warp >> 2;                    // keys [64*half, 64*half+64) of the tile
+    const int r = ((warp & 3) << 5) + lane;        // query row in the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float c = p.scale_log2;
+    const float nlog2e = -1.4426950408889634f;
+    uint8_t* sp = smem + L::P_OFF + half * 16384;
     uint8_t* sds = smem + L::DS_OFF + half * 16384;
+    // this row's -lse*log2(e) and D for a (head, query tile): rows past T give P = 0
+    auto load_row = [&](int bh, int qi, float& nl, float& dd) {
+      const int q = qi * BM + r;
+      const size_t i = (size_t)bh * T + q;
+      nl = q < T ? __ldg(p.lse + i) * nlog2e : -INFINITY;
+      dd = q < T ? __ldg(p.D + i) : 0.f;
+    };
+    float nl_next = 0.f, d_next = 0.f;
+    if (n_items_cta > 0) {
+      const BwdItem f = bwd_decode<CAUSAL>(bwd_item(0), p);
+      load_row(f.bh, f.i0, nl_next, d_next);
+    }
     int g = 0;
     bool ok = true;
     for (int ic = 0; ok && ic < n_items_cta; ++ic) {
       const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
-      const int key = w.kv * BN + r;
       for (int it = 0; it < w.n_it; ++it, ++g) {
-        const int st = g % BWD_STAGES;
         const int qi = w.i0 + it;
-        ok = mbar_wait(&bar_q_full[st], (g / BWD_STAGES) & 1, &abort_sh, gerr);
-        ok = ok && mbar_wait(&bar_sdp_full, g & 1, &abort_sh, gerr);
-        ok = __all_sync(0xffffffffu, ok);
+        const float nl = nl_next, dq = d_next;
+        // the row statistics of the next step, loaded one step ahead
+        if (it + 1 < w.n_it) {
+          load_row(w.bh, qi + 1, nl_next, d_next);
+        } else if (ic + 1 < n_items_cta) {
+          const BwdItem nx = bwd_decode<CAUSAL>(bwd_item(ic + 1), p);
+          load_row(nx.bh, nx.i0, nl_next, d_next);
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_sdp_full, g & 1, &abort_sh, gerr));
         if (!ok) break;
         tc_fence_after();
         uint32_t sv[2][32], dpv[2][32];
@@ -532,33 +530,40 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
         tmem_tie32(dpv[1]);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_sdp_free);   // S^T/dP^T columns may be overwritten now
-        const float* rs = reinterpret_cast<const float*>(smem + L::ROWST_OFF) + st * 256 + half * 64;
-        const bool diag = CAUSAL && (qi == w.kv);
+        if (lane == 0) mbar_arrive(&bar_sdp_free);   // S/dP columns may be overwritten now
+        // keys [kbase, kbase + lim) of this half are visible to the row
+        const int kbase = w.kv * BN + half * 64;
+        int lim = 64;
+        if (CAUSAL && qi == w.kv) lim = min(lim, r - half * 64 + 1);     // diagonal tile: key <= query
+        if (kbase + 64 > T) lim = min(lim, T - kbase);                   // keys past T
         uint32_t pk[32], dk[32];
-        // masked variant only on the diagonal tile or a tile with keys past T
-        if (__any_sync(0xffffffffu, diag || key >= T))
-          bwd_p_ds<true>(sv, dpv, rs, c, half * 64, r, diag, key < T, pk, dk);
+        if (__any_sync(0xffffffffu, lim < 64))
+          bwd_p_ds<true>(sv, dpv, nl, dq, c, lim, pk, dk);
         else
-          bwd_p_ds<false>(sv, dpv, rs, c, half * 64, r, false, true, pk, dk);
-        // dS^T row `r`, queries [64*half, 64*half+64): block `half`, 8 chunks of
-        // 16 bytes, once the previous step's dK and dQ have read the tile
+          bwd_p_ds<false>(sv, dpv, nl, dq, c, 64, pk, dk);
+        // dS into TMEM (A of dQ) and smem (A of dK), once the previous step's
+        // dK and dQ have read them
         if (g > 0) {
           ok = __all_sync(0xffffffffu, mbar_wait(&bar_ds_free, (g - 1) & 1, &abort_sh, gerr));
           if (!ok) break;
+          tc_fence_after();
         }
+        tmem_st32(tmem + lane_off + TB_DS + half * 32, dk);
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           const uint4 v = make_uint4(dk[ch * 4 + 0], dk[ch * 4 + 1], dk[ch * 4 + 2], dk[ch * 4 + 3]);
           *reinterpret_cast<uint4*>(sds + swz_chunk_offset<64>(r, ch)) = v;
         }
-        // P^T into TMEM once the previous step's dV has read it
+        // P into smem (A of dV) once the previous step's dV has read it
         if (g > 0) {
           ok = __all_sync(0xffffffffu, mbar_wait(&bar_p_free, (g - 1) & 1, &abort_sh, gerr));
           if (!ok) break;
-          tc_fence_after();
         }
-        tmem_st32(tmem + lane_off + TB_P + half * 32, pk);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 v = make_uint4(pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+          *reinterpret_cast<uint4*>(sp + swz_chunk_offset<64>(r, ch)) = v;
+        }
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();

@@ -13,6 +13,17 @@
 #ifndef ATTN_WAIT_NS
 #define ATTN_WAIT_NS 2000000000ull  // 2 s of wall time per wait
 #endif
+// Polls between two reads of the clock.
+#ifndef ATTN_WAIT_POLLS_PER_CHECK
+#define ATTN_WAIT_POLLS_PER_CHECK 64
+#endif
+// 1: poll with the non-blocking mbarrier.test_wait instead of try_wait (which
+// may suspend the thread until the phase completes). With ATTN_WAIT_NS = 0 and
+// one poll per check, every wait that does not complete at once gives up
+// within about a microsecond: a build for testing the kernels' wind-down.
+#ifndef ATTN_WAIT_NONBLOCKING
+#define ATTN_WAIT_NONBLOCKING 0
+#endif
 
 namespace attn {
 
@@ -86,11 +97,19 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   uint32_t ok;
+#if ATTN_WAIT_NONBLOCKING
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(addr), "r"(parity) : "memory");
+#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok) : "r"(addr), "r"(parity) : "memory");
+#endif
   return ok != 0;
 }
 
@@ -105,7 +124,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   uint32_t spins = 0;
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((++spins & 63u) == 0) {
+    if (++spins % ATTN_WAIT_POLLS_PER_CHECK == 0) {
       if (*abort_word) return false;
       if (globaltimer_ns() - t0 > ATTN_WAIT_NS) {
         *abort_word = 1;

@@ -8,8 +8,10 @@ attn_last_device_error, the word must be cleared by that read, and the
 context must stay usable for real work afterwards.
 
 The real forward and backward kernels are made to give up too: a copy of the
-library is built with a wait limit of zero (ATTN_WAIT_NS=0), so their first
-wait that does not complete at once runs out, in whichever role it happens.
+library is built with a wait limit of zero (ATTN_WAIT_NS=0), a clock read at
+every poll and non-blocking polls (mbarrier.test_wait; the product build's
+try_wait may suspend until the phase completes), so their first wait that is
+not over within about a microsecond runs out, in whichever role it happens.
 In a child process that copy runs a forward and a backward with several work
 items per CTA; each must return, the host must read ATTN_ERR_TIMEOUT once per
 call, and no CUDA error may follow. The parent then runs the normal library
@@ -111,7 +113,8 @@ def test_real_kernels_wind_down_when_their_waits_run_out(env):
         pytest.skip("no CUDA device")
     from causal_head_attention_fwd_gb300 import build
     root = pathlib.Path(__file__).resolve().parents[1]
-    lib = build.build(extra_flags=["-DATTN_WAIT_NS=0ull"], lib=root / "_build" / "zero_wait" / "libattn_zero_wait.so",
+    lib = build.build(extra_flags=["-DATTN_WAIT_NS=0ull", "-DATTN_WAIT_POLLS_PER_CHECK=1",
+                                                  "-DATTN_WAIT_NONBLOCKING=1"], lib=root / "_build" / "zero_wait" / "libattn_zero_wait.so",
                       build_dir=root / "_build" / "zero_wait")
     r = subprocess.run([sys.executable, "-c", _CHILD, str(lib)], capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-3000:]
