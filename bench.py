@@ -314,7 +314,7 @@ FP8_PER_BF16 = 4.5 / 2.25     # nominal dense e4m3 / bf16 tensor rate of the GB3
 
 
 def run_fp8(args):
-    """Times attn_fwd_fp8 (e4m3 qkv with per-tensor descales, bf16 out) on one
+    """Times attn_fwd_fp8 (e4m3 qkv with per-tile descales, bf16 out) on one
     GPU; FLOPs of the forward against the e4m3 tensor peak."""
     import torch
     from causal_head_attention_fwd_gb300 import build, inputs
@@ -323,7 +323,7 @@ def run_fp8(args):
     dev = torch.device("cuda", 0)
     w = inputs.FP8_WORKLOADS[args.fp8]
     B, T, C, NH, causal = w["B"], w["T"], w["C"], w["NH"], w["causal"]
-    f = inputs.make_fp8_inputs(B, T, C, sigma=w["sigma"], seed=w["seed"])
+    f = inputs.make_fp8_inputs(B, T, C, sigma=w["sigma"], seed=w["seed"], NH=NH)
     codes = torch.from_numpy(f.codes).to(dev)
     descale = torch.from_numpy(f.descale).to(dev)
     out = torch.empty((B, T, C), dtype=torch.bfloat16, device=dev)

@@ -182,7 +182,8 @@ def attn_decode(qkv, out, lse, B, L, C, NH, Tq, dtype, workspace, workspace_byte
 
 
 def attn_fwd_fp8(qkv, descale, out, lse, B, T, C, NH, causal, stream=None, check=True) -> int:
-    """e4m3 qkv codes with per-tensor descales (device, 3 fp32) -> bf16 out, fp32 lse."""
+    """e4m3 qkv codes with per-tile descales (device, (3, B, NH, ceil(T/128)) fp32)
+    -> bf16 out, fp32 lse."""
     st = _lib.attn_fwd_fp8(_ptr(qkv), _ptr(descale), _ptr(out), _ptr(lse), B, T, C, NH, int(causal),
                            _stream(stream))
     if check and st != ATTN_OK:

@@ -32,7 +32,7 @@ cudaError_t launch_bwd_f32(const CUtensorMap& map_q_l, const CUtensorMap& map_q_
 
 cudaError_t launch_fwd_fp8(const CUtensorMap& map_qkv, const CUtensorMap& map_out, const float* descale, float* lse,
                            const Problem& pr, cudaStream_t stream);
-cudaError_t launch_fp8_dequant(const void* codes, const float* descale, void* out, int B, int T, int C,
+cudaError_t launch_fp8_dequant(const void* codes, const float* descale, void* out, int B, int T, int C, int NH,
                                cudaStream_t stream);
 cudaError_t launch_linear(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
                           const void* bias, int M, int N, int K, cudaStream_t stream);
@@ -269,6 +269,9 @@ extern "C" int attn_fwd_schedule(int B, int T, int C, int NH, int n_cta, int* of
   return fwd_schedule(pr, n_cta, off, items, cap);
 }
 
+// Bytes of the FP8 descale array: 3 (q, k, v) x B*NH heads x ceil(T/128) row tiles, fp32.
+static size_t fp8_descale_bytes(int B, int T, int NH) { return (size_t)3 * B * NH * ((T + BM - 1) / BM) * 4; }
+
 extern "C" attn_status_t attn_fwd_fp8(const void* qkv, const float* descale, void* out, float* lse, int B, int T,
                                       int C, int NH, int causal, void* stream) {
   attn_status_t st = check_shape(B, T, C, NH, causal, ATTN_BF16);
@@ -276,7 +279,8 @@ extern "C" attn_status_t attn_fwd_fp8(const void* qkv, const float* descale, voi
   if (!qkv || !descale || !out || !lse) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(qkv) || !aligned16(out) || !aligned16(lse) || (reinterpret_cast<uintptr_t>(descale) & 3u))
     return ATTN_ERR_MISALIGNED;
-  const size_t nq = (size_t)B * T * 3 * C, no = (size_t)B * T * C * 2, nl = (size_t)B * NH * T * 4, nd = 3 * 4;
+  const size_t nq = (size_t)B * T * 3 * C, no = (size_t)B * T * C * 2, nl = (size_t)B * NH * T * 4;
+  const size_t nd = fp8_descale_bytes(B, T, NH);
   if (overlaps(out, no, qkv, nq) || overlaps(lse, nl, qkv, nq) || overlaps(lse, nl, out, no) ||
       overlaps(descale, nd, out, no) || overlaps(descale, nd, lse, nl))
     return ATTN_ERR_INVALID_ARG;
@@ -337,10 +341,11 @@ extern "C" attn_status_t attn_bwd_fp8(const void* dout, const void* qkv, const f
   if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_MISALIGNED;
   const size_t n8 = (size_t)B * T * 3 * C, n3 = n8 * 2, n1 = (size_t)B * T * C * 2, nl = (size_t)B * NH * T * 4;
+  const size_t nd = fp8_descale_bytes(B, T, NH);
   if (overlaps(dqkv, n3, qkv, n8) || overlaps(dqkv, n3, out, n1) || overlaps(dqkv, n3, dout, n1) ||
-      overlaps(dqkv, n3, lse, nl) || overlaps(dqkv, n3, descale, 12) || overlaps(workspace, need, qkv, n8) ||
+      overlaps(dqkv, n3, lse, nl) || overlaps(dqkv, n3, descale, nd) || overlaps(workspace, need, qkv, n8) ||
       overlaps(workspace, need, out, n1) || overlaps(workspace, need, dout, n1) ||
-      overlaps(workspace, need, lse, nl) || overlaps(workspace, need, descale, 12) ||
+      overlaps(workspace, need, lse, nl) || overlaps(workspace, need, descale, nd) ||
       overlaps(workspace, need, dqkv, n3))
     return ATTN_ERR_INVALID_ARG;
   if (!device_error_word() || device_sm_count() <= 0) return ATTN_ERR_CUDA;
@@ -348,7 +353,7 @@ extern "C" attn_status_t attn_bwd_fp8(const void* dout, const void* qkv, const f
   //    backward run in bf16), 2. the bf16 backward on them
   char* ws = static_cast<char*>(workspace);
   void* qkv16 = ws;
-  if (launch_fp8_dequant(qkv, descale, qkv16, B, T, C, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (launch_fp8_dequant(qkv, descale, qkv16, B, T, C, NH, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
   const size_t off = fp8_qkv_bytes(B, T, C);
   return attn_bwd(dout, qkv16, out, lse, dqkv, B, T, C, NH, causal, ATTN_BF16, ws + off, workspace_bytes - off,

@@ -2,14 +2,18 @@
 //
 // The lower-precision forward that "LLM Systems 10 & 11: Accelerating
 // Transformer Training and Inference", §1.3 (mixed-precision calculation)
-// allows next to FP16: q, k, v are stored as e4m3 with one fp32 descale each
-// (real value = code * descale), the two contractions run on the tensor core
-// as tcgen05.mma kind::f8f6f4 with fp32 accumulation, and out is bf16:
-//   s_tj  = dq dk (q8_t . k8_j)                      (exact fp32 sums of e4m3 products)
-//   p_tj  = exp(scale * s_tj - scale * m_t),  j in J(t)    (fp32, online)
-//   out_t = dv * sum_j e4m3(p_tj) v8_j / sum_j p_tj
-//   lse_t = scale * m_t + ln sum_j p_tj
-// The probabilities enter P.V as e4m3 codes (p <= 2^8 under the lazy
+// allows next to FP16: q, k, v are stored as e4m3 with one fp32 descale per
+// 128-row tile of each head (real value = code * descale of its tile), the two
+// contractions run on the tensor core as tcgen05.mma kind::f8f6f4 with fp32
+// accumulation, and out is bf16. For query tile a and key tile b of a head,
+// with dq_a, dk_b, dv_b the tiles' descales and dv* the largest dv_b the
+// query tile sees:
+//   y_tj  = scale log2(e) dq_a dk_b (q8_t . k8_j)     (exact fp32 sums of e4m3 products)
+//   p'_tj = 2^(y_tj - m_t) (dv_b / dv*),  j in J(t)    (fp32, online; r_b = dv_b/dv* <= 1
+//           folded into the exponent)
+//   out_t = dv* sum_j e4m3(p'_tj) v8_j / sum_j p'_tj / r_b
+//   lse_t = (m_t + log2 sum_j 2^(y_tj - m_t)) ln 2
+// The probabilities enter P.V as e4m3 codes (p' <= 2^8 under the lazy
 // rescaling below, inside e4m3's range of 448); the row sum uses the fp32 p.
 //
 // Same schedule as the bf16 forward (attention forward_cpu passes 1-4 of
@@ -91,9 +95,10 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float p0, float p1, float p2, fl
 
 struct Params {
   float* lse;
-  const float* descale;   // [3]: q, k, v
+  const float* descale;   // [3][B*NH][nT]: q, k, v descales per (head, 128-row tile)
   int* err;
   int T, NH, C;
+  int nT;                 // 128-row tiles per head = ceil(T / 128)
   int n_pairs, BH, n_items;
   float scale_log2;       // (1/sqrt(hs)) * log2(e)
 };
@@ -276,10 +281,8 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
     const uint32_t tP = tmem + lane_off + (wg ? TM_P1 : TM_P0);
     const uint32_t bar_id = 1 + wg;
     const bool leader = (warp & 3) == 0 && lane == 0;
-    // exponent scale of the raw e4m3 dot products, and the output descale
-    const float c = p.scale_log2 * __ldg(p.descale + 0) * __ldg(p.descale + 1);
-    const float dv = __ldg(p.descale + 2);
     uint8_t* stage = smem + L::OUT_OFF + wg * L::OUT_TILE;
+    const size_t dstride = (size_t)p.BH * p.nT;  // between the q, k and v descale planes
     bool ok = true;
     int gs = 0;
     for (int ic = 0; ok && ic < n_items_cta; ++ic) {
@@ -287,9 +290,20 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
       const int qb = ic & 1;
       const int n = w.n_tile[wg];
       const int t = w.q0 + wg * BM + r;
+      // descales of this head: q of this query tile; k and v per key tile
+      const float* dsc = p.descale + (size_t)(w.b * p.NH + w.h) * p.nT;
+      const float cq = n > 0 ? p.scale_log2 * __ldg(dsc + (w.q0 + wg * BM) / BM) : 0.f;
+      float dv_ref = 0.f;                        // the largest v descale the tile sees
+      for (int kt = 0; kt < n; ++kt) dv_ref = fmaxf(dv_ref, __ldg(dsc + 2 * dstride + kt));
+      const float lg_dv_ref = __log2f(dv_ref);
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < n; ++j) {
         const int gj = gs + j;
+        // this key tile: exponent scale of the raw e4m3 products, and
+        // log2(dv_j / dv*) <= 0, which puts V's descale into P
+        const float c = cq * __ldg(dsc + dstride + j);
+        const float dvj = __ldg(dsc + 2 * dstride + j);
+        const float a_j = __log2f(dvj) - lg_dv_ref;
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[wg], gj & 1, &abort_sh, gerr));
         if (!ok) break;
         tc_fence_after();
@@ -325,11 +339,13 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
           for (int e = 0; e < 32; e += 2)
             mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(s[q][e]), __uint_as_float(s[q][e + 1]));
         const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-        // lazy rescaling: the reference max moves only when the row max exceeds
-        // it by more than 8 (log2 units), so p <= 2^8 < 448 (e4m3 range)
-        const float m_new = (mx - m_run) * c > 8.f ? mx : m_run;
-        const float alpha = ex2_approx((m_run - m_new) * c);
-        const float2 c2 = make_float2(c, c), nmc = make_float2(-m_new * c, -m_new * c);
+        // lazy rescaling: the reference max (log2 units, as y = s * c) moves
+        // only when the row max exceeds it by more than 8, so p' <= p <= 2^8 < 448
+        // (e4m3 range)
+        const float my = mx * c;
+        const float m_new = my - m_run > 8.f ? my : m_run;
+        const float alpha = ex2_approx(m_run - m_new);
+        const float2 c2 = make_float2(c, c), nmc = make_float2(a_j - m_new, a_j - m_new);
         float2 ls[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -368,7 +384,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
         }
         if (!ok) break;
         const float lsum = ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
-        l_run = l_run * alpha + lsum;
+        l_run = l_run * alpha + lsum * ex2_approx(-a_j);   // the sum of p = p' / r_j
         m_run = m_new;
         tmem_st_wait();
         tc_fence_before();
@@ -382,7 +398,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
       if (n > 0) {
         const bool fail = !ok || !mbar_wait(&bar_pv[wg], (gs + n - 1) & 1, &abort_sh, gerr);
         tc_fence_after();
-        const float f = dv / l_run;
+        const float f = dv_ref / l_run;
         // the previous item's store of this staging tile must have read it
         if (leader) bulk_wait_group_read0();
         if (named_bar_red_or(bar_id, 128, fail)) { ok = false; break; }
@@ -401,7 +417,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
             *reinterpret_cast<uint4*>(stage + swz_chunk_offset<HS>(r, cc / 8 + ch)) = v;
           }
         }
-        if (t < T) p.lse[(size_t)(w.b * p.NH + w.h) * T + t] = (m_run * c + __log2f(l_run)) * 0.69314718055994531f;
+        if (t < T) p.lse[(size_t)(w.b * p.NH + w.h) * T + t] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
         fence_proxy_async_smem();
         named_bar_sync(bar_id, 128);
         if (leader) {
@@ -444,6 +460,7 @@ cudaError_t launch_fwd_fp8(const CUtensorMap& map_qkv, const CUtensorMap& map_ou
   f8::Params p;
   p.lse = lse;
   p.descale = descale;
+  p.nT = (pr.T + BM - 1) / BM;
   p.err = device_error_word();
   p.T = pr.T;
   p.NH = pr.NH;
@@ -467,16 +484,21 @@ cudaError_t launch_fwd_fp8(const CUtensorMap& map_qkv, const CUtensorMap& map_ou
 namespace attn {
 namespace f8 {
 
-// e4m3 codes -> bf16 values code * descale[part] (part = q, k, v by column),
-// 16 codes per thread: one 16-byte load, two 16-byte stores.
+// e4m3 codes -> bf16 values code * descale of the code's (part, head, 128-row
+// tile), 16 codes per thread: one 16-byte load, two 16-byte stores. The 16
+// codes of a thread lie in one head's slot (hs is a multiple of 16).
 __global__ void attn_fp8_dequant(const uint4* __restrict__ codes, const float* __restrict__ descale,
-                                 uint4* __restrict__ out, int C, long long n16) {
+                                 uint4* __restrict__ out, int T, int C, int NH, int BH, long long n16) {
   pdl_launch_and_wait();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n16) return;
   const long long e = i * 16;                              // element index in (B, T, 3C)
-  const int col = (int)(e % (3LL * C));
-  const float d = __ldg(descale + col / C);                // C % 16 == 0: one part per thread
+  const long long row = e / (3LL * C);                     // b * T + t
+  const int col = (int)(e - row * 3LL * C);
+  const int part = col / C, h = (col - part * C) / (C / NH);
+  const int b = (int)(row / T), t = (int)(row - (long long)b * T);
+  const int nT = (T + BM - 1) / BM;
+  const float d = __ldg(descale + ((size_t)part * BH + (size_t)b * NH + h) * nT + t / BM);
   const uint4 v = codes[i];
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t o[8];
@@ -500,13 +522,13 @@ __global__ void attn_fp8_dequant(const uint4* __restrict__ codes, const float* _
 
 }  // namespace f8
 
-cudaError_t launch_fp8_dequant(const void* codes, const float* descale, void* out, int B, int T, int C,
+cudaError_t launch_fp8_dequant(const void* codes, const float* descale, void* out, int B, int T, int C, int NH,
                                cudaStream_t stream) {
   const long long n16 = (long long)B * T * 3 * C / 16;
   const int threads = 256;
   const long long blocks = (n16 + threads - 1) / threads;
   return launch_pdl(f8::attn_fp8_dequant, dim3((unsigned)blocks), dim3(threads), 0, stream,
-                    static_cast<const uint4*>(codes), descale, static_cast<uint4*>(out), C, n16);
+                    static_cast<const uint4*>(codes), descale, static_cast<uint4*>(out), T, C, NH, B * NH, n16);
 }
 
 }  // namespace attn

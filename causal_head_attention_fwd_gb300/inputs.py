@@ -190,26 +190,54 @@ def e4m3_decode(code: np.ndarray) -> np.ndarray:
 
 @dataclasses.dataclass
 class Fp8Inputs:
-    """qkv as e4m3 codes with one descale per q, k, v (value = code * descale)."""
+    """qkv as e4m3 codes with one descale per 128-row tile of each head's q, k
+    and v (value = code * descale of its tile)."""
     codes: np.ndarray        # (B, T, 3C) uint8
-    descale: np.ndarray      # (3,) float32
+    descale: np.ndarray      # (3, B, NH, ceil(T/128)) float32
     qkv: np.ndarray          # (B, T, 3C) float64, the exact values the codes stand for
 
 
-def make_fp8_inputs(B, T, C, sigma=0.5, seed=1) -> Fp8Inputs:
-    """Draw qkv ~ N(0, sigma^2) (the bf16 recipe's normals), pick each tensor's
-    descale so its largest magnitude maps to the largest e4m3 code, quantise."""
+FP8_TILE = 128
+
+
+def fp8_tile_view(x: np.ndarray, C: int, NH: int, part: int):
+    """Tiles of part (0 q, 1 k, 2 v) of x (B, T, 3C): yields (b, h, tile, slice)
+    with slice selecting rows [128*tile, 128*tile+128) of that head's columns."""
+    B, T, _ = x.shape
+    hs = C // NH
+    for b in range(B):
+        for h in range(NH):
+            c0 = part * C + h * hs
+            for k in range((T + FP8_TILE - 1) // FP8_TILE):
+                yield b, h, k, (b, slice(k * FP8_TILE, min(T, (k + 1) * FP8_TILE)), slice(c0, c0 + hs))
+
+
+def make_fp8_inputs(B, T, C, sigma=0.5, seed=1, NH=None, tile_gain=False) -> Fp8Inputs:
+    """Draw qkv ~ N(0, sigma^2) (the bf16 recipe's normals), pick each tile's
+    descale so its largest magnitude maps to the largest e4m3 code (a tile is
+    128 rows of one head's q, k or v), quantise. NH defaults to C / 64. With
+    tile_gain, every tile is first multiplied by 2^u, u uniform in [-1, 1]
+    (drawn from seed + 1), so the tiles' descales differ by up to 4x."""
+    NH = NH if NH is not None else C // 64
     x = normal_f64(seed, B * T * 3 * C).reshape(B, T, 3 * C) * sigma
+    nT = (T + FP8_TILE - 1) // FP8_TILE
+    if tile_gain:
+        w = _splitmix64(seed + 1, 0, 3 * B * NH * nT)
+        u = ((w >> np.uint64(11)).astype(np.float64) + 0.5) / 9007199254740992.0
+        gain = np.exp2(2.0 * u - 1.0).reshape(3, B, NH, nT)
+        for part in range(3):
+            for b, h, k, sl in fp8_tile_view(x, C, NH, part):
+                x[sl] *= gain[part, b, h, k]
     codes = np.empty(x.shape, dtype=np.uint8)
-    descale = np.empty(3, dtype=np.float32)
-    for i in range(3):
-        part = x[:, :, i * C:(i + 1) * C]
-        d = np.float32(max(float(np.max(np.abs(part))), 1e-30) / E4M3_MAX)
-        descale[i] = d
-        codes[:, :, i * C:(i + 1) * C] = e4m3_encode(part / float(d))
-    vals = e4m3_decode(codes)
-    for i in range(3):
-        vals[:, :, i * C:(i + 1) * C] *= float(descale[i])
+    vals = np.empty(x.shape, dtype=np.float64)
+    descale = np.empty((3, B, NH, nT), dtype=np.float32)
+    for part in range(3):
+        for b, h, k, sl in fp8_tile_view(x, C, NH, part):
+            tile = x[sl]
+            d = np.float32(max(float(np.max(np.abs(tile))), 1e-30) / E4M3_MAX)
+            descale[part, b, h, k] = d
+            codes[sl] = e4m3_encode(tile / float(d))
+            vals[sl] = e4m3_decode(codes[sl]) * float(d)
     return Fp8Inputs(codes, descale, vals)
 
 

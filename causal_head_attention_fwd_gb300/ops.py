@@ -91,10 +91,11 @@ def attention_forward(qkv: torch.Tensor, n_head: int, causal: bool = True, out=N
 
 def attention_forward_fp8(qkv_e4m3: torch.Tensor, descale: torch.Tensor, n_head: int, causal: bool = True,
                           out=None, lse=None, stream=None):
-    """e4m3 qkv codes (uint8, (B, T, 3C)) and per-tensor descales (3 fp32 on the
-    device) -> out (B, T, C) bf16 and lse (B, NH, T) fp32."""
+    """e4m3 qkv codes (uint8, (B, T, 3C)) and per-tile descales ((3, B, NH,
+    ceil(T/128)) fp32 on the device: q, k, v of each head's 128-row tiles)
+    -> out (B, T, C) bf16 and lse (B, NH, T) fp32."""
     B, T, C, NH = _shape(qkv_e4m3, n_head, dtypes=(torch.uint8,))
-    _expect(descale, "descale", (3,), torch.float32)
+    _expect(descale, "descale", (3, B, NH, (T + 127) // 128), torch.float32)
     _expect(out, "out", (B, T, C), torch.bfloat16)
     _expect(lse, "lse", (B, NH, T), torch.float32)
     _on_device(qkv_e4m3, descale=descale, out=out, lse=lse)

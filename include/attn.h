@@ -66,23 +66,27 @@ attn_status_t attn_fwd(const void* qkv, void* out, float* lse, int B, int T, int
  * Accelerating Transformer Training and Inference" §1.3 (mixed-precision
  * calculation) names for the forward next to FP16.
  *   qkv     : (B, T, 3C) e4m3 codes (one byte each), llm.c's layout, read only.
- *   descale : device array of 3 fp32, read only: the real value of a code of
- *             q, k, v is code * descale[0], [1], [2] (one scale per tensor).
+ *   descale : device array (3, B, NH, nT) fp32, nT = ceil(T/128), read only:
+ *             one scale per 128-row tile of each head's q, k and v. The code
+ *             of part i (0 q, 1 k, 2 v) of head h at row t of sequence b
+ *             stands for code * descale[((i*B + b)*NH + h)*nT + t/128]. Every
+ *             entry must be positive and finite (not checked: device data).
  *   out     : (B, T, C) bf16, fully overwritten.
  *   lse     : (B, NH, T) fp32, fully overwritten (natural log, scaled scores).
  * q.k and P.V run on the tensor core in e4m3 with fp32 accumulation; the
  * softmax probabilities enter P.V as e4m3 codes (relative rounding error at
- * most 2^-4), the row sums and lse are formed from the fp32 probabilities.
- * hs in {32, 64}; qkv, out, lse 16-byte aligned, descale 4-byte aligned; no
- * buffer may overlap another (ATTN_ERR_INVALID_ARG).
+ * most 2^-4; each key tile's v descale relative to the largest one the query
+ * tile sees is folded into them), the row sums and lse are formed from the
+ * fp32 probabilities. hs in {32, 64}; qkv, out, lse 16-byte aligned, descale
+ * 4-byte aligned; no buffer may overlap another (ATTN_ERR_INVALID_ARG).
  */
 attn_status_t attn_fwd_fp8(const void* qkv, const float* descale, void* out, float* lse, int B, int T, int C,
                            int NH, int causal, void* stream);
 
 /*
  * FP8 backward: gradients of attn_fwd_fp8's attention with respect to the
- * real q, k, v values (code * descale). The e4m3 codes are expanded to bf16
- * on the GPU (code * descale, rounded once to bf16) and the bf16 backward
+ * real q, k, v values (code * its tile's descale). The e4m3 codes are expanded
+ * to bf16 on the GPU (code * descale, rounded once to bf16) and the bf16 backward
  * (attn_bwd) runs on them: its matmuls are bf16 on the tensor core, not e4m3.
  *   dout, out : (B, T, C) bf16 (out as attn_fwd_fp8 wrote it); lse from attn_fwd_fp8.
  *   qkv, descale : as for attn_fwd_fp8.

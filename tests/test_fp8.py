@@ -1,7 +1,8 @@
 """FP8 (e4m3) forward and backward against the oracle on the dequantised inputs.
 
-The e4m3 codes stand for exact values (code * descale), so the oracle runs the
-plain float64 forward on those values. The kernel's only coarse rounding is the
+The e4m3 codes stand for exact values (code * the descale of the code's
+128-row tile of its head's q, k or v), so the oracle runs the plain float64
+forward on those values. The kernel's only coarse rounding is the
 probabilities entering P.V as e4m3 codes (relative error <= 2^-4 each); the
 scores are exact sums of e4m3 products in fp32, the row sums and lse use the
 fp32 probabilities, and out is rounded to bf16 (2^-9). Hence, per output:
@@ -57,11 +58,18 @@ def test_e4m3_round_trip_and_rounding():
 
 
 def test_fp8_inputs_dequantise_to_the_codes():
-    f = inputs.make_fp8_inputs(2, 8, 64, sigma=0.5, seed=7)
-    for i in range(3):
-        part = inputs.e4m3_decode(f.codes[:, :, i * 64:(i + 1) * 64]) * float(f.descale[i])
-        assert np.array_equal(part, f.qkv[:, :, i * 64:(i + 1) * 64])
-        assert np.max(np.abs(f.codes[:, :, i * 64:(i + 1) * 64] & 0x7F)) == 0x7E   # full range used
+    B, T, C, NH = 2, 300, 128, 2
+    for gain in (False, True):
+        f = inputs.make_fp8_inputs(B, T, C, sigma=0.5, seed=7, NH=NH, tile_gain=gain)
+        assert f.descale.shape == (3, B, NH, 3)
+        for part in range(3):
+            for b, h, k, sl in inputs.fp8_tile_view(f.codes, C, NH, part):
+                d = float(f.descale[part, b, h, k])
+                assert np.array_equal(inputs.e4m3_decode(f.codes[sl]) * d, f.qkv[sl])
+                assert np.max(f.codes[sl] & 0x7F) == 0x7E          # each tile uses the full range
+    # the gains make the tiles' scales differ
+    g = inputs.make_fp8_inputs(B, T, C, sigma=0.5, seed=7, NH=NH, tile_gain=True).descale
+    assert g.max() / g.min() > 2.0
 
 
 # ----------------------------------------------------------------------------- ABI
@@ -82,6 +90,9 @@ def test_fp8_rejects_bad_arguments():
     assert call(causal=3) == api.ATTN_ERR_INVALID_ARG
     assert call(out=A + 1024) == api.ATTN_ERR_INVALID_ARG          # out overlaps qkv
     assert call(d=A + 2 * S + 64) == api.ATTN_ERR_INVALID_ARG      # descale inside out
+    # the descale array spans 3 * B * NH * ceil(T/128) floats (48 bytes here):
+    # one that starts 32 bytes before out runs into it
+    assert call(d=A + 2 * S - 32) == api.ATTN_ERR_INVALID_ARG
 
 
 # ----------------------------------------------------------------------------- GPU parity
@@ -130,8 +141,9 @@ def _check_head(g_out, g_lse, qkv, b, h, T, C, NH, causal):
     (1, 700, 128, 2, 0),      # non-causal ragged
     (1, 1000, 64, 1, 1),      # one head, eight tiles
 ])
-def test_fp8_forward_matches_oracle(env, B, T, C, NH, causal):
-    f = inputs.make_fp8_inputs(B, T, C, sigma=0.5, seed=77 + T)
+@pytest.mark.parametrize("gain", [False, True])
+def test_fp8_forward_matches_oracle(env, B, T, C, NH, causal, gain):
+    f = inputs.make_fp8_inputs(B, T, C, sigma=0.5, seed=77 + T, NH=NH, tile_gain=gain)
     g_out, g_lse = _run(env, f, B, T, C, NH, causal)
     for b in range(B):
         for h in range(NH):
@@ -144,7 +156,7 @@ def test_fp8_gpt2s_workload_all_heads(env):
     the oracle on the dequantised inputs, and the whole output written."""
     w = inputs.FP8_WORKLOADS["gpt2s_fp8"]
     B, T, C, NH = w["B"], w["T"], w["C"], w["NH"]
-    f = inputs.make_fp8_inputs(B, T, C, sigma=w["sigma"], seed=w["seed"])
+    f = inputs.make_fp8_inputs(B, T, C, sigma=w["sigma"], seed=w["seed"], NH=NH)
     g_out, g_lse = _run(env, f, B, T, C, NH, w["causal"])
     assert np.isfinite(g_out).all() and np.isfinite(g_lse).all()
     for b in range(B):
@@ -193,7 +205,7 @@ def _bwd_fp8(env, f, out_bits, lse_f32, dout_bits, B, T, C, NH):
 @pytest.mark.parametrize("B,T,C,NH", [(2, 64, 128, 4), (1, 300, 128, 2), (1, 1000, 64, 1)])
 def test_fp8_backward_given_exact_forward(env, B, T, C, NH):
     """out and lse from the oracle: the GPU backward must meet the bf16 rule (2e-2 * max|ref| per q/k/v)."""
-    f = inputs.make_fp8_inputs(B, T, C, sigma=0.5, seed=91 + T)
+    f = inputs.make_fp8_inputs(B, T, C, sigma=0.5, seed=91 + T, NH=NH, tile_gain=True)
     r_out, r_lse = oracle.forward(f.qkv, B, T, C, NH, True)
     dout, dout_bits = inputs.draw((B, T, C), 1e-2, 92 + T, "bf16")
     out_bits = inputs.f32_to_bf16_bits(r_out.astype(np.float32))
@@ -212,7 +224,7 @@ def test_fp8_forward_then_backward(env, B, T, C, NH):
     the forward's measured error), |err dq_t| <= 2e-2 max|dq| + scale |dD_t| sum_j att_tj |k_j| and
     |err dk_j| <= 2e-2 max|dk| + scale sum_t att_tj |dD_t| |q_t|."""
     torch, api, ops = env
-    f = inputs.make_fp8_inputs(B, T, C, sigma=0.5, seed=93 + T)
+    f = inputs.make_fp8_inputs(B, T, C, sigma=0.5, seed=93 + T, NH=NH, tile_gain=True)
     g_out, g_lse = _run(env, f, B, T, C, NH, 1)
     dout, dout_bits = inputs.draw((B, T, C), 1e-2, 94 + T, "bf16")
     out_bits = inputs.f32_to_bf16_bits(g_out.astype(np.float32))   # exact: g_out holds bf16 values
