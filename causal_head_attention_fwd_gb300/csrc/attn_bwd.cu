@@ -15,7 +15,8 @@
 // Three launches on the caller's stream:
 //   1. attn_bwd_pre:    D (fp32, (B,NH,T)) and zero the fp32 dq accumulator (B,T,C)
 //   2. attn_bwd_kernel: persistent, one CTA per SM. Work item = (128-key tile,
-//      b, h); a CTA walks its items (heavy causal key tiles first, dealt in a
+//      b, h); a CTA walks its items (causal items dealt longest first, each to
+//      the CTA with the least work so far, as the forward's; otherwise in a
 //      snake order over the CTAs) and, per item, the query tiles that see
 //      those keys. S^T, dP^T, dV, dK, dQ on tcgen05; dQ tiles are added into
 //      the accumulator with TMA bulk reductions; dK/dV stored by TMA.
@@ -45,6 +46,7 @@
 // TMEM columns: S [0,128) dP [128,256) dV [256,320) dK [320,384) dQ [384,448)
 //               dS [448,512) (bf16 pairs)
 #include "common.cuh"
+#include "fwd_deal.cuh"
 
 namespace attn {
 
@@ -86,13 +88,6 @@ struct BwdParams {
   float scale;        // 1/sqrt(hs)
   float scale_log2;   // scale * log2(e)
 };
-
-// Work item k of a CTA: rounds of gridDim.x items, snake order (even rounds
-// left to right, odd rounds right to left) so heavy and light items pair up.
-__device__ __forceinline__ int bwd_item(int k) {
-  const int G = gridDim.x, c = blockIdx.x;
-  return k * G + ((k & 1) ? (G - 1 - c) : c);
-}
 
 struct BwdItem {
   int kv, bh, b, h, i0, n_it;
@@ -205,7 +200,7 @@ template <int HS, bool CAUSAL>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_dout,
                 const __grid_constant__ CUtensorMap map_dqkv, const __grid_constant__ CUtensorMap map_dqacc,
-                const BwdParams p) {
+                const BwdParams p, const __grid_constant__ WorkDeal sched) {
   using G = TileGeom<HS>;
   using L = BwdSmem<HS>;
   extern __shared__ uint8_t smem_raw[];
@@ -213,8 +208,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
 
   __shared__ uint64_t bar_k_full[2], bar_k_empty[2], bar_v_full, bar_v_empty;
   __shared__ uint64_t bar_q_full[BWD_STAGES], bar_q_empty[BWD_STAGES];
-  __shared__ uint64_t bar_sdp_full, bar_sdp_free, bar_pds_full, bar_ds_free, bar_p_free, bar_dq_full, bar_dq_free,
-      bar_done, bar_epi_free;
+  __shared__ uint64_t bar_sdp_full, bar_sdp_free, bar_pds_full, bar_ds_free, bar_p_free, bar_dq_free, bar_done,
+      bar_epi_free;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
 
@@ -222,13 +217,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
   const int lane = threadIdx.x & 31;
   const int T = p.T;
   // this CTA's items and total number of steps (query tiles over all items)
-  int n_items_cta = 0, total_g = 0;
-  for (int k = 0;; ++k) {
-    const int idx = bwd_item(k);
-    if (idx >= p.n_items) break;
-    ++n_items_cta;
-    total_g += bwd_decode<CAUSAL>(idx, p).n_it;
-  }
+  const int n_items_cta = deal_count(sched, p.n_items);
+  int total_g = 0;
+  for (int k = 0; k < n_items_cta; ++k) total_g += bwd_decode<CAUSAL>(deal_item(sched, k), p).n_it;
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
@@ -245,9 +236,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
     mbar_init(&bar_sdp_full, 1);
     mbar_init(&bar_sdp_free, 8);                 // one arrival per P/dS warp
     mbar_init(&bar_pds_full, 8);
-    mbar_init(&bar_ds_free, 1);                  // dK and dQ of the step read dS (smem and TMEM)
+    mbar_init(&bar_ds_free, 1);                  // dK and dQ of the step done: dQ ready, dS free
     mbar_init(&bar_p_free, 1);                   // dV of the step read P
-    mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_free, 4);                  // one arrival per dQ warp
     mbar_init(&bar_done, 1);
     mbar_init(&bar_epi_free, 4);
@@ -274,7 +264,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
         bool ok = true;
         int g = 0;
         for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-          const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
+          const BwdItem w = bwd_decode<CAUSAL>(deal_item(sched, ic), p);
           const int kb = ic & 1;
           if (ic >= 2 && !(ok = mbar_wait(&bar_k_empty[kb], ((ic >> 1) - 1) & 1, &abort_sh, gerr))) break;
           mbar_arrive_expect_tx(&bar_k_full[kb], G::TILE_BYTES);
@@ -295,7 +285,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
       // ------------------------------------------------------------ loader: V
       if (lane == 0) {
         for (int ic = 0; ic < n_items_cta; ++ic) {
-          const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
+          const BwdItem w = bwd_decode<CAUSAL>(deal_item(sched, ic), p);
           // the previous item's dP steps must be done with the buffer
           if (ic >= 1 && !mbar_wait(&bar_v_empty, (ic - 1) & 1, &abort_sh, gerr)) break;
           mbar_arrive_expect_tx(&bar_v_full, G::TILE_BYTES);
@@ -339,10 +329,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
 #pragma unroll
           for (int k = 0; k < BN / 16; ++k)
             mma_ts(tmem + TB_DQ, tmem + TB_DS + k * 8, desc_add(kd, k * 16 * G::ROW_BYTES), id_dq, k > 0);
-          mma_commit(&bar_dq_full);
-          // dS (smem and TMEM) is free once dK and dQ are done: the next one is
-          // written while dV still runs (only commits that someone waits for)
-          if (f.g + 1 < total_g) mma_commit(&bar_ds_free);
+          // dQ is ready and dS (smem and TMEM) free once dK and dQ are done: the
+          // dQ warps drain dQ and the P/dS warps write the next dS while dV runs
+          mma_commit(&bar_ds_free);
           // dV += P^T dO
 #pragma unroll
           for (int k = 0; k < BM / 16; ++k)
@@ -360,7 +349,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
         bool have_pend = false;
         int g = 0;
         for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-          const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
+          const BwdItem w = bwd_decode<CAUSAL>(deal_item(sched, ic), p);
           const int kb = ic & 1;
           if (!(ok = mbar_wait(&bar_k_full[kb], (ic >> 1) & 1, &abort_sh, gerr))) break;
           if (!(ok = mbar_wait(&bar_v_full, ic & 1, &abort_sh, gerr))) break;
@@ -399,12 +388,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
       int g = 0;
       bool ok = true;
       for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-        const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
+        const BwdItem w = bwd_decode<CAUSAL>(deal_item(sched, ic), p);
         for (int it = 0; it < w.n_it; ++it, ++g) {
           const int qi = w.i0 + it;
           // failures are combined over the warpgroup at the first barrier, so a
           // bounded wait that gave up never leaves a thread stuck at a barrier
-          const bool fail = !mbar_wait(&bar_dq_full, g & 1, &abort_sh, gerr);
+          const bool fail = !mbar_wait(&bar_ds_free, g & 1, &abort_sh, gerr);
           tc_fence_after();
           // one 32-column block at a time: TMEM -> 16 KB staging tile -> reduce;
           // the dQ columns are released once the last block is in registers
@@ -438,45 +427,61 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
         }
         if (!ok) break;
         // ---------------------------------------------------------- dK, dV of this item
+        // dV goes to the staging tile and scale*dK to registers (bf16 pairs)
+        // before either is stored, so the TMEM columns are handed back to the
+        // next item's first dK and dV without waiting for the stores.
         const bool fail = !mbar_wait(&bar_done, ic & 1, &abort_sh, gerr);
         tc_fence_after();
-        // dV, then scale*dK, through the staging tile
+        if (leader) bulk_wait_group_read0();             // staging free
+        if (named_bar_red_or(1, 128, fail)) { ok = false; break; }
+        uint8_t* stage = sdq;
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          if (leader) bulk_wait_group_read0();           // staging free
-          if (named_bar_red_or(1, 128, fail)) { ok = false; break; }
-          const uint32_t col = which == 0 ? TB_DV : TB_DK;
-          const float mul = which == 0 ? 1.f : s;
-          uint8_t* stage = sdq;
-#pragma unroll
-          for (int cc = 0; cc < HS; cc += 32) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_off + col + cc, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(o[ch * 8 + 0]) * mul, __uint_as_float(o[ch * 8 + 1]) * mul);
-              v.y = pack_bf16x2(__uint_as_float(o[ch * 8 + 2]) * mul, __uint_as_float(o[ch * 8 + 3]) * mul);
-              v.z = pack_bf16x2(__uint_as_float(o[ch * 8 + 4]) * mul, __uint_as_float(o[ch * 8 + 5]) * mul);
-              v.w = pack_bf16x2(__uint_as_float(o[ch * 8 + 6]) * mul, __uint_as_float(o[ch * 8 + 7]) * mul);
-              *reinterpret_cast<uint4*>(stage + swz_chunk_offset<HS>(r, cc / 8 + ch)) = v;
-            }
-          }
-          if (which == 1) {
-            tc_fence_before();
-            // every commit is awaited: only signal if the MMA warp will wait for it
-            __syncwarp();
-            if (lane == 0 && ic + 1 < n_items_cta) mbar_arrive(&bar_epi_free);   // dK/dV TMEM columns free
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(1, 128);
-          if (leader) {
-            tma_store_3d(&map_dqkv, stage, (which == 0 ? 2 * p.C : p.C) + w.h * HS, w.kv * BN, w.b);
-            bulk_commit_group();
-          }
+        for (int cc = 0; cc < HS; cc += 16) {
+          uint32_t o[16];
+          tmem_ld16_wait(tmem + lane_off + TB_DV + cc, o);
+          uint4 v0, v1;
+          v0.x = pack_bf16x2(__uint_as_float(o[0]), __uint_as_float(o[1]));
+          v0.y = pack_bf16x2(__uint_as_float(o[2]), __uint_as_float(o[3]));
+          v0.z = pack_bf16x2(__uint_as_float(o[4]), __uint_as_float(o[5]));
+          v0.w = pack_bf16x2(__uint_as_float(o[6]), __uint_as_float(o[7]));
+          v1.x = pack_bf16x2(__uint_as_float(o[8]), __uint_as_float(o[9]));
+          v1.y = pack_bf16x2(__uint_as_float(o[10]), __uint_as_float(o[11]));
+          v1.z = pack_bf16x2(__uint_as_float(o[12]), __uint_as_float(o[13]));
+          v1.w = pack_bf16x2(__uint_as_float(o[14]), __uint_as_float(o[15]));
+          *reinterpret_cast<uint4*>(stage + swz_chunk_offset<HS>(r, cc / 8)) = v0;
+          *reinterpret_cast<uint4*>(stage + swz_chunk_offset<HS>(r, cc / 8 + 1)) = v1;
         }
-        if (!ok) break;
+        uint32_t dkp[HS / 2];
+#pragma unroll
+        for (int cc = 0; cc < HS; cc += 16) {
+          uint32_t o[16];
+          tmem_ld16_wait(tmem + lane_off + TB_DK + cc, o);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dkp[cc / 2 + e] = pack_bf16x2(__uint_as_float(o[2 * e]) * s, __uint_as_float(o[2 * e + 1]) * s);
+        }
+        tc_fence_before();
+        // every commit is awaited: only signal if the MMA warp will wait for it
+        __syncwarp();
+        if (lane == 0 && ic + 1 < n_items_cta) mbar_arrive(&bar_epi_free);   // dK/dV TMEM columns free
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader) {
+          tma_store_3d(&map_dqkv, stage, 2 * p.C + w.h * HS, w.kv * BN, w.b);
+          bulk_commit_group();
+          bulk_wait_group_read0();                       // staging free again
+        }
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int ch = 0; ch < HS / 8; ++ch)
+          *reinterpret_cast<uint4*>(stage + swz_chunk_offset<HS>(r, ch)) =
+              make_uint4(dkp[ch * 4 + 0], dkp[ch * 4 + 1], dkp[ch * 4 + 2], dkp[ch * 4 + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader) {
+          tma_store_3d(&map_dqkv, stage, p.C + w.h * HS, w.kv * BN, w.b);
+          bulk_commit_group();
+        }
       }
       if (leader) bulk_wait_group0();
     }
@@ -499,13 +504,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
     };
     float nl_next = 0.f, d_next = 0.f;
     if (n_items_cta > 0) {
-      const BwdItem f = bwd_decode<CAUSAL>(bwd_item(0), p);
+      const BwdItem f = bwd_decode<CAUSAL>(deal_item(sched, 0), p);
       load_row(f.bh, f.i0, nl_next, d_next);
     }
     int g = 0;
     bool ok = true;
     for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-      const BwdItem w = bwd_decode<CAUSAL>(bwd_item(ic), p);
+      const BwdItem w = bwd_decode<CAUSAL>(deal_item(sched, ic), p);
       for (int it = 0; it < w.n_it; ++it, ++g) {
         const int qi = w.i0 + it;
         const float nl = nl_next, dq = d_next;
@@ -513,7 +518,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
         if (it + 1 < w.n_it) {
           load_row(w.bh, qi + 1, nl_next, d_next);
         } else if (ic + 1 < n_items_cta) {
-          const BwdItem nx = bwd_decode<CAUSAL>(bwd_item(ic + 1), p);
+          const BwdItem nx = bwd_decode<CAUSAL>(deal_item(sched, ic + 1), p);
           load_row(nx.bh, nx.i0, nl_next, d_next);
         }
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_sdp_full, g & 1, &abort_sh, gerr));
@@ -586,13 +591,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
 // ----------------------------------------------------------------------------
 template <int HS, bool CAUSAL>
 static cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& md, const CUtensorMap& mg,
-                                   const CUtensorMap& macc, const BwdParams& p, int grid,
+                                   const CUtensorMap& macc, const BwdParams& p, const WorkDeal& deal, int grid,
                                    cudaStream_t stream) {
   auto k = attn_bwd_kernel<HS, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdSmem<HS>::ALLOC);
   if (e != cudaSuccess) return e;
   ProfileScope ps(K_BWD_MAIN, stream);
-  return launch_pdl(k, dim3(grid), dim3(BWD_THREADS), BwdSmem<HS>::ALLOC, stream, mq, md, mg, macc, p);
+  return launch_pdl(k, dim3(grid), dim3(BWD_THREADS), BwdSmem<HS>::ALLOC, stream, mq, md, mg, macc, p, deal);
 }
 
 cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_dout,
@@ -625,12 +630,13 @@ cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_d
   p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)pr.hs));
   const int n_sm = device_sm_count();
   const int grid = p.n_items < n_sm ? p.n_items : n_sm;   // persistent: one CTA per SM
+  const WorkDeal deal = launch_deal_bwd(pr.causal, p.n_kv, p.BH, grid);
   if (pr.hs == 64)
-    e = pr.causal ? launch_bwd_main<64, true>(map_qkv, map_dout, map_dqkv, map_dqacc, p, grid, stream)
-                  : launch_bwd_main<64, false>(map_qkv, map_dout, map_dqkv, map_dqacc, p, grid, stream);
+    e = pr.causal ? launch_bwd_main<64, true>(map_qkv, map_dout, map_dqkv, map_dqacc, p, deal, grid, stream)
+                  : launch_bwd_main<64, false>(map_qkv, map_dout, map_dqkv, map_dqacc, p, deal, grid, stream);
   else
-    e = pr.causal ? launch_bwd_main<32, true>(map_qkv, map_dout, map_dqkv, map_dqacc, p, grid, stream)
-                  : launch_bwd_main<32, false>(map_qkv, map_dout, map_dqkv, map_dqacc, p, grid, stream);
+    e = pr.causal ? launch_bwd_main<32, true>(map_qkv, map_dout, map_dqkv, map_dqacc, p, deal, grid, stream)
+                  : launch_bwd_main<32, false>(map_qkv, map_dout, map_dqkv, map_dqacc, p, deal, grid, stream);
   if (e != cudaSuccess) return e;
 
   ProfileScope ps(K_BWD_DQ, stream);

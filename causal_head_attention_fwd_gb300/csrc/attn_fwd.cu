@@ -144,8 +144,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
       tma_prefetch_desc(&map_qkv);
       bool ok = true;
       int gk = 0;                                 // key-tile steps so far
+      FwdItem w_next = n_items_cta > 0 ? fwd_decode<CAUSAL>(deal_item(sched, 0), p) : FwdItem{};
       for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-        const FwdItem w = fwd_decode<CAUSAL>(deal_item(sched, ic), p);
+        const FwdItem w = w_next;                 // decoded one item ahead
+        if (ic + 1 < n_items_cta) w_next = fwd_decode<CAUSAL>(deal_item(sched, ic + 1), p);
         const int qb = ic & 1;
         if (ic >= 2 && !(ok = mbar_wait(&bar_q_empty[qb], ((ic >> 1) - 1) & 1, &abort_sh, gerr))) break;
         const uint32_t qbytes = (w.n_tile[0] > 0 ? G::TILE_BYTES : 0) + (w.n_tile[1] > 0 ? G::TILE_BYTES : 0);
@@ -197,8 +199,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
       bool ok = true;
       int gk = 0;                                 // key-tile steps so far
       int gs = 0;                                 // softmax steps of this query tile so far
+      FwdItem w_next = n_items_cta > 0 ? fwd_decode<CAUSAL>(deal_item(sched, 0), p) : FwdItem{};
       for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-        const FwdItem w = fwd_decode<CAUSAL>(deal_item(sched, ic), p);
+        const FwdItem w = w_next;                 // decoded one item ahead
+        if (ic + 1 < n_items_cta) w_next = fwd_decode<CAUSAL>(deal_item(sched, ic + 1), p);
         const int qb = ic & 1;
         const int n = w.n_tile[i];
         // first scores of the item, once the softmax warps hold the previous S_i
@@ -250,8 +254,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
     const float c = p.scale_log2;
     bool ok = true;
     int gs = 0;                                  // softmax steps of this tile so far
+    int q_pending = -1;                          // Q buffer still to hand back
+    auto release_q = [&]() {
+      if (q_pending >= 0 && leader) {
+        bulk_wait_group_read0();
+        mbar_arrive(&bar_q_empty[q_pending]);
+      }
+      q_pending = -1;
+    };
+    FwdItem w_next = n_items_cta > 0 ? fwd_decode<CAUSAL>(deal_item(sched, 0), p) : FwdItem{};
     for (int ic = 0; ok && ic < n_items_cta; ++ic) {
-      const FwdItem w = fwd_decode<CAUSAL>(deal_item(sched, ic), p);
+      const FwdItem w = w_next;                  // decoded one item ahead
+      if (ic + 1 < n_items_cta) w_next = fwd_decode<CAUSAL>(deal_item(sched, ic + 1), p);
       const int qb = ic & 1;
       const int n = w.n_tile[wg];
       const int t = w.q0 + wg * BM + r;          // query row
@@ -344,6 +358,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_p[wg]);
+        if (j == 0) release_q();
       }
       // -------------------------------------------------------- epilogue of this item
       // A warp whose wait gave up left the key loop early, but it still comes
@@ -378,13 +393,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
         if (leader) {
           tma_store_3d(&map_out, stage, w.h * HS, w.q0 + wg * BM, w.b);
           bulk_commit_group();
-          bulk_wait_group_read0();                 // the staging (Q) tile may be reloaded
         }
       }
-      // hand the Q buffer back to the producer if it will reload it
-      if (leader && ic + 2 < n_items_cta) mbar_arrive(&bar_q_empty[qb]);
+      release_q();
+      if (ic + 2 < n_items_cta) q_pending = qb;
       gs += n;
     }
+    if (leader) bulk_wait_group0();
   }
 
   tc_fence_before();

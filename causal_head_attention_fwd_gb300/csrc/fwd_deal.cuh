@@ -1,4 +1,4 @@
-// Deal of the forward kernels' work items over their persistent CTAs.
+// Deal of the persistent kernels' work items over their CTAs.
 //
 // A work item is two 128-row query tiles of one (b, h); item idx starts at
 // query row 2*BM*(n_pairs-1-idx/BH) of head idx%BH, so low indices are the
@@ -7,6 +7,8 @@
 // work so far (greedy longest-processing-time), and passes every CTA's list in
 // the launch parameters. Without a table (too many items, or equal items when
 // non-causal) CTA c takes items c, 2G-1-c, 2G+c, ... in rounds of G CTAs.
+// The backward deals its causal items (one key tile of one head each) the
+// same way.
 #pragma once
 #include <algorithm>
 #include <functional>
@@ -52,12 +54,12 @@ inline int causal_item_steps(int idx, int n_pairs, int BH, int T) {
   return n;
 }
 
-// Greedy longest-processing-time deal of the causal items over `grid` CTAs.
-// An item weighs its key steps plus 1.7 for its start-up (measured: ~4k
-// cycles from an item's last P to the next item's first scores, against
-// ~2.4k per key step).
-inline void build_causal_deal(WorkDeal& s, int n_pairs, int BH, int T, int grid) {
-  const int n_items = n_pairs * BH;
+// Greedy longest-processing-time deal of n_items items over `grid` CTAs:
+// items in index order (the callers number them longest first), each to the
+// CTA with the least work so far; cost(idx) is an item's work in key-tile
+// steps, `overhead` its start-up in the same unit.
+template <typename Cost>
+inline void build_lpt_deal(WorkDeal& s, int n_items, int grid, float overhead, Cost cost) {
   s.use = 0;
   if (n_items > DEAL_MAX_ITEMS || grid < 1 || grid > DEAL_MAX_CTAS) return;
   using Load = std::pair<float, int>;      // (work so far, CTA): least work, then lowest CTA
@@ -68,7 +70,7 @@ inline void build_causal_deal(WorkDeal& s, int n_pairs, int BH, int T, int grid)
     const Load l = heap.top();
     heap.pop();
     per[l.second].push_back(idx);
-    heap.push({l.first + (float)causal_item_steps(idx, n_pairs, BH, T) + 1.7f, l.second});
+    heap.push({l.first + (float)cost(idx) + overhead, l.second});
   }
   int n = 0;
   for (int c = 0; c < grid; ++c) {
@@ -77,6 +79,14 @@ inline void build_causal_deal(WorkDeal& s, int n_pairs, int BH, int T, int grid)
   }
   s.off[grid] = (uint16_t)n;
   s.use = 1;
+}
+
+// The forward's causal items: an item weighs its key steps plus 1.7 for its
+// start-up (measured: ~4k cycles from an item's last P to the next item's
+// first scores, against ~2.4k per key step).
+inline void build_causal_deal(WorkDeal& s, int n_pairs, int BH, int T, int grid) {
+  build_lpt_deal(s, n_pairs * BH, grid, 1.7f,
+                 [&](int idx) { return causal_item_steps(idx, n_pairs, BH, T); });
 }
 
 // The deal a launch uses: the causal table (built once per shape, then
@@ -93,6 +103,27 @@ inline WorkDeal launch_deal(bool causal, int n_pairs, int BH, int T, int grid) {
   if (!std::equal(key, key + 4, key0)) {
     build_causal_deal(cached, n_pairs, BH, T, grid);
     std::copy(key, key + 4, key0);
+  }
+  return cached;
+}
+
+// The backward's causal deal: item idx = key tile idx / BH of head idx % BH
+// walks the query tiles from that key tile on, n_kv - idx / BH steps (key tile
+// 0 first); an item weighs its steps plus 0.5 for its start-up (the first
+// step's K/V wait and the previous item's dK/dV hand-over). Built once per
+// shape; the snake order when the items are equal (no mask) or too many.
+inline WorkDeal launch_deal_bwd(bool causal, int n_kv, int BH, int grid) {
+  WorkDeal d;
+  d.use = 0;
+  if (!causal) return d;
+  static std::mutex mu;
+  static WorkDeal cached;
+  static long long key0[3] = {-1, -1, -1};
+  const long long key[3] = {n_kv, BH, grid};
+  std::lock_guard<std::mutex> lk(mu);
+  if (!std::equal(key, key + 3, key0)) {
+    build_lpt_deal(cached, n_kv * BH, grid, 0.5f, [&](int idx) { return n_kv - idx / BH; });
+    std::copy(key, key + 3, key0);
   }
   return cached;
 }
