@@ -732,14 +732,24 @@ def main(argv=None):
 # CUDA sources each kernel is compiled from (its translation unit and headers)
 _KERNEL_SOURCES = {
     "attn_fwd_kernel": ["attn_fwd.cu", "fwd_deal.cuh", "common.cuh", "ptx.cuh"],
-    "attn_bwd_kernel": ["attn_bwd.cu", "common.cuh", "ptx.cuh"],
+    "attn_bwd_kernel": ["attn_bwd.cu", "fwd_deal.cuh", "common.cuh", "ptx.cuh"],
     "f32": ["attn_f32.cu", "tf32.cuh", "common.cuh", "ptx.cuh"],
 }
 
 
+def _code_only(text: str) -> str:
+    """C++ source with its comments and blank lines taken out, so that a change
+    to a comment keeps a kernel's hash."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
 def kernel_source_hash(kernel: str = "attn_bwd_kernel") -> str:
-    """Hash of the CUDA sources a kernel is built from; ties a stored ncu
-    traffic figure to the kernel version it measured."""
+    """Hash of the code (comments excluded) of the CUDA sources a kernel is
+    built from; ties a stored ncu traffic figure to the kernel version it
+    measured."""
     import hashlib
     h = hashlib.sha256()
     csrc = ROOT / "causal_head_attention_fwd_gb300" / "csrc"
@@ -748,7 +758,7 @@ def kernel_source_hash(kernel: str = "attn_bwd_kernel") -> str:
         return ""
     for name in names:
         h.update(name.encode())
-        h.update((csrc / name).read_bytes())
+        h.update(_code_only((csrc / name).read_text()).encode())
     return h.hexdigest()[:16]
 
 

@@ -14,11 +14,11 @@
 // Persistent: one CTA per SM. Work item = two 128-row query tiles of one
 // (b, h) (256 rows); a CTA walks its items longest first (causal items are
 // dealt by the host, each to the CTA with the least work so far; otherwise in
-// a snake order over the CTAs). 10 warps:
+// a snake order over the CTAs). 12 warps:
 //   warps 0-3  softmax warpgroup for query tile 0 (TMEM lanes 0-127)
 //   warps 4-7  softmax warpgroup for query tile 1
 //   warp  8    TMA producer: Q (double-buffered per item), K/V tiles through
-//              a 3-stage ring that runs on across items
+//              a 4-stage ring that runs on across items
 //   warps 9-10 MMA issuers, one thread per query tile; warp 11 idle
 //   (setmaxnreg: 208 registers for the softmax warpgroups, 80 for warps 8-11)
 // S_i(j+1) is issued as soon as the softmax warps of tile i hold S_i(j) in
