@@ -137,7 +137,8 @@ size_t attn_bwd_workspace_size(int B, int T, int C, int NH, int causal, attn_dty
  *   workspace : device buffer of at least attn_bwd_workspace_size(...) bytes,
  *          256-byte aligned, owned by the caller; contents on entry do not
  *          matter and are garbage on return. Must not overlap any other
- *          buffer (ATTN_ERR_INVALID_ARG).
+ *          buffer (ATTN_ERR_INVALID_ARG). Calls whose GPU work overlaps in
+ *          time (other streams) need workspaces of their own.
  */
 attn_status_t attn_bwd(const void* dout, const void* qkv, const void* out, const float* lse,
                        void* dqkv, int B, int T, int C, int NH, int causal, attn_dtype_t dtype,

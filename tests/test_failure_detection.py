@@ -116,7 +116,7 @@ def test_real_kernels_wind_down_when_their_waits_run_out(env):
     lib = build.build(extra_flags=["-DATTN_WAIT_NS=0ull", "-DATTN_WAIT_POLLS_PER_CHECK=1",
                                                   "-DATTN_WAIT_NONBLOCKING=1"], lib=root / "_build" / "zero_wait" / "libattn_zero_wait.so",
                       build_dir=root / "_build" / "zero_wait")
-    r = subprocess.run([sys.executable, "-c", _CHILD, str(lib)], capture_output=True, text=True, timeout=600)
+    r = subprocess.run([sys.executable, "-c", _CHILD, str(lib)], capture_output=True, text=True, timeout=180)
     assert r.returncode == 0, r.stderr[-3000:]
     res = json.loads(r.stdout.strip().splitlines()[-1])
     assert res["fwd_status"] == api.ATTN_OK and res["bwd_status"] == api.ATTN_OK     # launched
