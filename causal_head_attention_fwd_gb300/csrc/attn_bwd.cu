@@ -161,6 +161,10 @@ __global__ void attn_bwd_dq_out(const float4* __restrict__ dq_acc, uint4* __rest
   v.z = pack_bf16x2(b.x, b.y);
   v.w = pack_bf16x2(b.z, b.w);
   dqkv[(bt * 3 * C + c) / 8] = v;
+  // The accumulator is dead now: drop its 128-byte lines from L2 without
+  // writing them back (four threads read one line; n_vec is a multiple of 4).
+  __syncwarp(__activemask());
+  if ((i & 3) == 0) l2_discard128(dq_acc + 2 * i);
 }
 
 // ----------------------------------------------------------------------------

@@ -70,6 +70,12 @@ __device__ __forceinline__ bool named_bar_red_or(uint32_t id, uint32_t nthreads,
   return r != 0;
 }
 
+// Drop the 128-byte L2 line at p (128-byte aligned) without writing it back;
+// its contents become undefined.
+__device__ __forceinline__ void l2_discard128(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" :: "l"(p) : "memory");
+}
+
 // --------------------------------------------------------------------------
 // mbarrier
 // --------------------------------------------------------------------------
