@@ -125,9 +125,11 @@ __global__ void attn_bwd_pre(const uint4* __restrict__ dout, const uint4* __rest
       acc = fmaf(__uint_as_float(aw[w] << 16), __uint_as_float(ow[w] << 16), acc);
       acc = fmaf(__uint_as_float(aw[w] & 0xFFFF0000u), __uint_as_float(ow[w] & 0xFFFF0000u), acc);
     }
+    // the accumulator has 2 * n_vec float4s: zero two of them, each store
+    // coalesced across the warp
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    dq_acc[2 * i] = z;
-    dq_acc[2 * i + 1] = z;
+    dq_acc[i] = z;
+    dq_acc[i + n_vec] = z;
   }
   // reduce across the LANES threads of one head row (aligned groups in the warp)
 #pragma unroll
