@@ -21,6 +21,7 @@ ATTN_ERR_MISALIGNED = 3
 ATTN_ERR_WORKSPACE = 4
 ATTN_ERR_CUDA = 5
 ATTN_ERR_TIMEOUT = 6
+ATTN_ERR_BOUNDS = 7
 
 ATTN_F32 = 0
 ATTN_BF16 = 1
@@ -53,7 +54,13 @@ def _load() -> ctypes.CDLL:
     if not _LIB_PATH.exists():
         raise ImportError(f"libattn.so not built at {_LIB_PATH}; run "
                           "`python -m causal_head_attention_fwd_gb300.build` (needs nvcc)")
-    lib = ctypes.CDLL(str(_LIB_PATH))
+    return configure(ctypes.CDLL(str(_LIB_PATH)))
+
+
+def configure(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the argument and result types of every entry point on a loaded
+    build of the library (this package's, or another build of the same
+    sources, e.g. with different compile flags)."""
     vp, i, f_p, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
     lib.attn_fwd.argtypes = [vp, vp, f_p, i, i, i, i, i, i, vp]
     lib.attn_fwd.restype = i

@@ -226,6 +226,7 @@ extern "C" const char* attn_status_string(attn_status_t s) {
     case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: workspace missing or too small";
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA call or launch failed";
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a kernel's bounded wait expired";
+    case ATTN_ERR_BOUNDS: return "ATTN_ERR_BOUNDS: a kernel index check failed (debug build)";
   }
   return "ATTN_ERR_UNKNOWN";
 }
@@ -522,7 +523,8 @@ extern "C" attn_status_t attn_last_device_error(void* stream) {
         cudaStreamSynchronize(s) != cudaSuccess)
       return ATTN_ERR_CUDA;
   }
-  return v == 0 ? ATTN_OK : (v == ATTN_ERR_TIMEOUT ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA);
+  if (v == 0) return ATTN_OK;
+  return (v == ATTN_ERR_TIMEOUT || v == ATTN_ERR_BOUNDS) ? static_cast<attn_status_t>(v) : ATTN_ERR_CUDA;
 }
 
 extern "C" attn_status_t attn_profile_enable(int enable) {

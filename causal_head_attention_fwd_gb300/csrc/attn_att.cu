@@ -124,7 +124,8 @@ attn_att_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
   const int t = qt * BM + r;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
   if (ok) {
-    const float lse2 = t < T ? p.lse[(size_t)bh * T + t] * 1.4426950408889634f : 0.f;
+    const bool in = t < T && ATTN_IN_RANGE((size_t)bh * T + t < (size_t)p.BH * T, gerr);
+    const float lse2 = in ? p.lse[(size_t)bh * T + t] * 1.4426950408889634f : 0.f;
     const float c = p.scale_log2;
     float* mats[2] = {p.preatt, p.att};
     const CUtensorMap* maps[2] = {&map_pre, &map_att};
@@ -178,6 +179,10 @@ attn_att_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
             const int rr = i >> 3, c4 = (i & 7) * 4;
             const int tg = qt * BM + rr, jg = j0 + c4;
             if (tg >= T || jg >= T) continue;
+            // the last of the four values stays inside the (B, NH, T, T) matrix
+            if (!ATTN_IN_RANGE(((size_t)bh * T + tg) * (size_t)T + jg + (jg + 3 < T ? 3 : T - 1 - jg) <
+                               (size_t)p.BH * T * (size_t)T, gerr))
+              continue;
             float* g = dst + ((size_t)bh * T + tg) * (size_t)T + jg;
 #pragma unroll
             for (int x = 0; x < 4; ++x)

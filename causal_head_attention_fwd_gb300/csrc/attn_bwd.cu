@@ -112,7 +112,7 @@ __device__ __forceinline__ BwdItem bwd_decode(int idx, const BwdParams& p) {
 template <int HS>
 __global__ void attn_bwd_pre(const uint4* __restrict__ dout, const uint4* __restrict__ out,
                              float* __restrict__ D, float4* __restrict__ dq_acc, int T, int C, int NH,
-                             long long n_vec) {
+                             long long n_vec, int* err) {
   pdl_launch_and_wait();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   constexpr int LANES = HS / 8;   // threads per head row
@@ -141,7 +141,8 @@ __global__ void attn_bwd_pre(const uint4* __restrict__ dout, const uint4* __rest
     const int h = c / HS;
     const long long b = bt / T;
     const int t = (int)(bt - b * T);
-    D[(b * NH + h) * T + t] = acc;
+    const long long di = (b * NH + h) * T + t;
+    if (ATTN_IN_RANGE(di < n_vec * 8 / C * NH, err)) D[di] = acc;   // D has B*T*NH entries
   }
 }
 
@@ -149,7 +150,7 @@ __global__ void attn_bwd_pre(const uint4* __restrict__ dout, const uint4* __rest
 // 3. dq accumulator (fp32, already scaled) -> bf16 into dqkv[:, :, 0:C].
 // ----------------------------------------------------------------------------
 __global__ void attn_bwd_dq_out(const float4* __restrict__ dq_acc, uint4* __restrict__ dqkv, int C,
-                                long long n_vec) {
+                                long long n_vec, int* err) {
   pdl_launch_and_wait();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // 8 channels each
   if (i >= n_vec) return;
@@ -162,7 +163,8 @@ __global__ void attn_bwd_dq_out(const float4* __restrict__ dq_acc, uint4* __rest
   v.y = pack_bf16x2(a.z, a.w);
   v.z = pack_bf16x2(b.x, b.y);
   v.w = pack_bf16x2(b.z, b.w);
-  dqkv[(bt * 3 * C + c) / 8] = v;
+  const long long oi = (bt * 3 * C + c) / 8;
+  if (ATTN_IN_RANGE(oi < 3 * n_vec, err)) dqkv[oi] = v;              // dqkv has 3 * n_vec 16-byte chunks
   // The accumulator is dead now: drop its 128-byte lines from L2 without
   // writing them back (four threads read one line; n_vec is a multiple of 4).
   __syncwarp(__activemask());
@@ -504,8 +506,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
     auto load_row = [&](int bh, int qi, float& nl, float& dd) {
       const int q = qi * BM + r;
       const size_t i = (size_t)bh * T + q;
-      nl = q < T ? __ldg(p.lse + i) * nlog2e : -INFINITY;
-      dd = q < T ? __ldg(p.D + i) : 0.f;
+      const bool in = q < T && ATTN_IN_RANGE(i < (size_t)p.BH * T, gerr);
+      nl = in ? __ldg(p.lse + i) * nlog2e : -INFINITY;
+      dd = in ? __ldg(p.D + i) : 0.f;
     };
     float nl_next = 0.f, d_next = 0.f;
     if (n_items_cta > 0) {
@@ -617,7 +620,7 @@ cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_d
     ProfileScope ps(K_BWD_PRE, stream);
     e = launch_pdl(pr.hs == 64 ? attn_bwd_pre<64> : attn_bwd_pre<32>, dim3((unsigned)blocks), dim3(threads), 0,
                    stream, static_cast<const uint4*>(dout), static_cast<const uint4*>(out), ws_D,
-                   reinterpret_cast<float4*>(ws_dq), pr.T, pr.C, pr.NH, n_vec);
+                   reinterpret_cast<float4*>(ws_dq), pr.T, pr.C, pr.NH, n_vec, device_error_word());
   }
   if (e != cudaSuccess) return e;
 
@@ -646,7 +649,8 @@ cudaError_t launch_bwd_bf16(const CUtensorMap& map_qkv, const CUtensorMap& map_d
 
   ProfileScope ps(K_BWD_DQ, stream);
   return launch_pdl(attn_bwd_dq_out, dim3((unsigned)blocks), dim3(threads), 0, stream,
-                    reinterpret_cast<const float4*>(ws_dq), static_cast<uint4*>(dqkv), pr.C, n_vec);
+                    reinterpret_cast<const float4*>(ws_dq), static_cast<uint4*>(dqkv), pr.C, n_vec,
+                    device_error_word());
 }
 
 }  // namespace attn

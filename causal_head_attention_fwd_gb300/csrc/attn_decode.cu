@@ -40,6 +40,7 @@ struct Params {
   float* part;                          // [B*NH][n_split][Tq][HS + 2]: m, l, o[HS]
   int* err;
   int L, C, NH, Tq, n_split;
+  int BH;                               // B * NH
   float scale_log2;
 };
 
@@ -143,6 +144,9 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
   const int j0 = split * CH;
   const int nk = min(CH, L - j0);
   const int g = tid / LPR, db = (tid % LPR) * 8;   // row group, first of this lane's 8 columns
+  // (b, h) of this CTA inside the batch: then every q row and record index is
+  // (the same decision in every thread, taken before any barrier)
+  if (!ATTN_IN_RANGE(bh < p.BH && L >= Tq && Tq <= TQ, p.err)) return;
   // the whole chunk of K and of V, one bulk tensor copy each (rows past L read
   // as zero); V lands while the scores and the softmax are computed
   if (tid == 0) {
@@ -296,6 +300,7 @@ __global__ void __launch_bounds__(HS) attn_decode_combine(const Params p) {
   const int Tq = p.Tq;
   // only chunks that hold a visible key of this query contribute
   const int last = (p.L - Tq + i) / Chunk<E>::N;
+  if (!ATTN_IN_RANGE(bh < p.BH && last < p.n_split && d < HS, p.err)) return;
   const float* rec = p.part + (size_t)bh * p.n_split * Tq * (HS + 2) + i * (HS + 2);
   float M = -INFINITY;
   for (int s = 0; s <= last; ++s) M = fmaxf(M, rec[(size_t)s * Tq * (HS + 2)]);
@@ -353,6 +358,7 @@ cudaError_t launch_decode(const CUtensorMap& map_qkv, const void* qkv, void* out
   p.NH = NH;
   p.Tq = Tq;
   p.n_split = (L + decode_chunk(f32) - 1) / decode_chunk(f32);
+  p.BH = B * NH;
   const int hs = C / NH;
   p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)hs));
   const int BH = B * NH;

@@ -399,7 +399,8 @@ attn_fwd_f32_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         tmem_ld_wait(o);
         stage32(stage, r, cc, o, inv_l);
       }
-      if (t < T && !fail) p.lse[(size_t)bh * T + t] = (m_run * c + __log2f(l_run)) * 0.69314718055994531f;
+      if (t < T && !fail && ATTN_IN_RANGE((size_t)bh * T + t < (size_t)p.BH * T, gerr))
+        p.lse[(size_t)bh * T + t] = (m_run * c + __log2f(l_run)) * 0.69314718055994531f;
       fence_proxy_async_smem();
       if (!named_bar_red_or(1 + wg, 128, fail) && leader) {
         store_tile<HS>(&map_out, stage, h * HS, q0 + wg * BQ, b);
@@ -425,7 +426,7 @@ attn_fwd_f32_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
 template <int HS>
 __global__ void __launch_bounds__(256)
 attn_bwd_pre_f32(const float* __restrict__ dout, const float* __restrict__ out, float* __restrict__ D, int T,
-                 int C, int NH, long long n_threads) {
+                 int C, int NH, long long n_threads, int* err) {
   constexpr int LANES = HS / 4;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const bool valid = i < n_threads;
@@ -442,7 +443,8 @@ attn_bwd_pre_f32(const float* __restrict__ dout, const float* __restrict__ out, 
   for (int off = LANES / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   if (valid && (ch % HS) == 0) {
     const long long bb = row / T, t = row % T;
-    D[(bb * NH + ch / HS) * T + t] = s;
+    const long long di = (bb * NH + ch / HS) * T + t;
+    if (ATTN_IN_RANGE(di < n_threads * 4 / C * NH, err)) D[di] = s;   // D has B*T*NH entries
   }
 }
 
@@ -646,8 +648,9 @@ attn_bwd_dkdv_f32(const __grid_constant__ CUtensorMap map_kv, const __grid_const
       {
         const int q = q0 + (r & 63);
         float v;
-        if (r < 64) v = q < T ? __ldg(lse_h + q) * LOG2E : INFINITY;
-        else v = q < T ? __ldg(D_h + q) : 0.f;
+        const bool in = q < T && ATTN_IN_RANGE((size_t)bh * T + q < (size_t)p.BH * T, gerr);
+        if (r < 64) v = in ? __ldg(lse_h + q) * LOG2E : INFINITY;
+        else v = in ? __ldg(D_h + q) : 0.f;
         rows[bb * 128 + r] = v;
       }
       // the barrier also shares a failure of any warp, so all leave together
@@ -887,8 +890,9 @@ attn_bwd_dq_f32(const __grid_constant__ CUtensorMap map_ql, const __grid_constan
     const int t = q0 + r;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const float c = p.scale_log2;
-    const float lse2 = t < T ? __ldg(p.lse + (size_t)bh * T + t) * LOG2E : 0.f;
-    const float Dt = t < T ? __ldg(p.D + (size_t)bh * T + t) : 0.f;
+    const bool in = t < T && ATTN_IN_RANGE((size_t)bh * T + t < (size_t)p.BH * T, gerr);
+    const float lse2 = in ? __ldg(p.lse + (size_t)bh * T + t) * LOG2E : 0.f;
+    const float Dt = in ? __ldg(p.D + (size_t)bh * T + t) : 0.f;
     const float2 c2 = make_float2(c, c), nl2 = make_float2(-lse2, -lse2), nd2 = make_float2(-Dt, -Dt);
     bool ok = true;
     for (int j = 0; j < n_k; ++j) {
@@ -976,7 +980,8 @@ static cudaError_t bwd_t(const CUtensorMap& q_l, const CUtensorMap& q_s, const C
   {
     ProfileScope ps(K_BWD_PRE, s);
     const long long n = (long long)pr.B * pr.T * pr.C / 4;
-    attn_bwd_pre_f32<HS><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(dout, out, ws_D, pr.T, pr.C, pr.NH, n);
+    attn_bwd_pre_f32<HS><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(dout, out, ws_D, pr.T, pr.C, pr.NH, n,
+                                                                    device_error_word());
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   BwdParams p = p0;

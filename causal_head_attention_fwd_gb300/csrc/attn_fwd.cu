@@ -384,9 +384,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
             *reinterpret_cast<uint4*>(stage + swz_chunk_offset<HS>(r, cc / 8 + ch)) = v;
           }
         }
-        if (t < T && !fail) {
+        const size_t li = (size_t)(w.b * p.NH + w.h) * T + t;
+        if (t < T && !fail && ATTN_IN_RANGE(li < (size_t)p.BH * T, gerr)) {
           // lse = scale*m + ln(l) = (m*c + log2 l) * ln 2
-          p.lse[(size_t)(w.b * p.NH + w.h) * T + t] = (m_run * c + __log2f(l_run)) * 0.69314718055994531f;
+          p.lse[li] = (m_run * c + __log2f(l_run)) * 0.69314718055994531f;
         }
         fence_proxy_async_smem();
         if (named_bar_red_or(bar_id, 128, fail)) { ok = false; break; }

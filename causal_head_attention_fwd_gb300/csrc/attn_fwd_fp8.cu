@@ -290,19 +290,22 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
       const int qb = ic & 1;
       const int n = w.n_tile[wg];
       const int t = w.q0 + wg * BM + r;
-      // descales of this head: q of this query tile; k and v per key tile
+      // descales of this head: q of this query tile; k and v per key tile (the
+      // head and its tiles lie inside the (3, B*NH, nT) array)
       const float* dsc = p.descale + (size_t)(w.b * p.NH + w.h) * p.nT;
-      const float cq = n > 0 ? p.scale_log2 * __ldg(dsc + (w.q0 + wg * BM) / BM) : 0.f;
+      const bool dsc_in =
+          ATTN_IN_RANGE(w.b * p.NH + w.h < p.BH && (n == 0 || (w.q0 + wg * BM) / BM < p.nT) && n <= p.nT, gerr);
+      const float cq = n > 0 && dsc_in ? p.scale_log2 * __ldg(dsc + (w.q0 + wg * BM) / BM) : 0.f;
       float dv_ref = 0.f;                        // the largest v descale the tile sees
-      for (int kt = 0; kt < n; ++kt) dv_ref = fmaxf(dv_ref, __ldg(dsc + 2 * dstride + kt));
+      for (int kt = 0; kt < n && dsc_in; ++kt) dv_ref = fmaxf(dv_ref, __ldg(dsc + 2 * dstride + kt));
       const float lg_dv_ref = __log2f(dv_ref);
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < n; ++j) {
         const int gj = gs + j;
         // this key tile: exponent scale of the raw e4m3 products, and
         // log2(dv_j / dv*) <= 0, which puts V's descale into P
-        const float c = cq * __ldg(dsc + dstride + j);
-        const float dvj = __ldg(dsc + 2 * dstride + j);
+        const float c = dsc_in ? cq * __ldg(dsc + dstride + j) : 0.f;
+        const float dvj = dsc_in ? __ldg(dsc + 2 * dstride + j) : 1.f;
         const float a_j = __log2f(dvj) - lg_dv_ref;
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[wg], gj & 1, &abort_sh, gerr));
         if (!ok) break;
@@ -417,7 +420,8 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
             *reinterpret_cast<uint4*>(stage + swz_chunk_offset<HS>(r, cc / 8 + ch)) = v;
           }
         }
-        if (t < T) p.lse[(size_t)(w.b * p.NH + w.h) * T + t] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+        if (t < T && ATTN_IN_RANGE((size_t)(w.b * p.NH + w.h) * T + t < (size_t)p.BH * T, gerr))
+          p.lse[(size_t)(w.b * p.NH + w.h) * T + t] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
         fence_proxy_async_smem();
         named_bar_sync(bar_id, 128);
         if (leader) {
@@ -488,7 +492,7 @@ namespace f8 {
 // tile), 16 codes per thread: one 16-byte load, two 16-byte stores. The 16
 // codes of a thread lie in one head's slot (hs is a multiple of 16).
 __global__ void attn_fp8_dequant(const uint4* __restrict__ codes, const float* __restrict__ descale,
-                                 uint4* __restrict__ out, int T, int C, int NH, int BH, long long n16) {
+                                 uint4* __restrict__ out, int T, int C, int NH, int BH, long long n16, int* err) {
   pdl_launch_and_wait();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n16) return;
@@ -498,7 +502,9 @@ __global__ void attn_fp8_dequant(const uint4* __restrict__ codes, const float* _
   const int part = col / C, h = (col - part * C) / (C / NH);
   const int b = (int)(row / T), t = (int)(row - (long long)b * T);
   const int nT = (T + BM - 1) / BM;
-  const float d = __ldg(descale + ((size_t)part * BH + (size_t)b * NH + h) * nT + t / BM);
+  const size_t di = ((size_t)part * BH + (size_t)b * NH + h) * nT + t / BM;
+  if (!ATTN_IN_RANGE(di < 3 * (size_t)BH * nT, err)) return;
+  const float d = __ldg(descale + di);
   const uint4 v = codes[i];
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t o[8];
@@ -528,7 +534,8 @@ cudaError_t launch_fp8_dequant(const void* codes, const float* descale, void* ou
   const int threads = 256;
   const long long blocks = (n16 + threads - 1) / threads;
   return launch_pdl(f8::attn_fp8_dequant, dim3((unsigned)blocks), dim3(threads), 0, stream,
-                    static_cast<const uint4*>(codes), descale, static_cast<uint4*>(out), T, C, NH, B * NH, n16);
+                    static_cast<const uint4*>(codes), descale, static_cast<uint4*>(out), T, C, NH, B * NH, n16,
+                    device_error_word());
 }
 
 }  // namespace attn

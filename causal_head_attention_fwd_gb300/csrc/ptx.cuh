@@ -24,6 +24,15 @@
 #ifndef ATTN_WAIT_NONBLOCKING
 #define ATTN_WAIT_NONBLOCKING 0
 #endif
+// Debug build (compiled with -DATTN_CHECK): the kernels test the index of each
+// plain global load and store against its buffer's extent; an index out of
+// range records ATTN_ERR_BOUNDS (7) in the device error word and the access is
+// skipped (a load yields 0). In a normal build the tests compile away.
+#ifdef ATTN_CHECK
+#define ATTN_IN_RANGE(cond, err) (::attn::check_range((cond), (err)))
+#else
+#define ATTN_IN_RANGE(cond, err) (true)
+#endif
 
 namespace attn {
 
@@ -75,6 +84,13 @@ __device__ __forceinline__ bool named_bar_red_or(uint32_t id, uint32_t nthreads,
 __device__ __forceinline__ void l2_discard128(const void* p) {
   asm volatile("discard.global.L2 [%0], 128;" :: "l"(p) : "memory");
 }
+
+#ifdef ATTN_CHECK
+__device__ __forceinline__ bool check_range(bool in_range, int* err) {
+  if (!in_range && err) atomicCAS(err, 0, 7 /* ATTN_ERR_BOUNDS */);
+  return in_range;
+}
+#endif
 
 // --------------------------------------------------------------------------
 // mbarrier

@@ -45,7 +45,10 @@ typedef enum {
   ATTN_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
   ATTN_ERR_WORKSPACE = 4,     /* backward workspace missing or too small */
   ATTN_ERR_CUDA = 5,          /* a CUDA runtime/driver call or launch failed */
-  ATTN_ERR_TIMEOUT = 6        /* a kernel's bounded wait expired (see attn_last_device_error) */
+  ATTN_ERR_TIMEOUT = 6,       /* a kernel's bounded wait expired (see attn_last_device_error) */
+  ATTN_ERR_BOUNDS = 7         /* debug build (-DATTN_CHECK) only: a kernel computed an index
+                                 outside a buffer and skipped that access (see
+                                 attn_last_device_error) */
 } attn_status_t;
 
 typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype_t;
@@ -188,8 +191,10 @@ const char* attn_status_string(attn_status_t status);
 
 /*
  * Synchronises `stream`, then reads and clears the device error word that the
- * kernels set when a bounded wait expires. Returns ATTN_OK, ATTN_ERR_TIMEOUT,
- * or ATTN_ERR_CUDA if the synchronisation itself failed.
+ * kernels set when a bounded wait expires (or, in a library built with
+ * -DATTN_CHECK, when a kernel's index check fails). Returns ATTN_OK,
+ * ATTN_ERR_TIMEOUT, ATTN_ERR_BOUNDS, or ATTN_ERR_CUDA if the synchronisation
+ * itself failed.
  */
 attn_status_t attn_last_device_error(void* stream);
 

@@ -62,7 +62,8 @@ def test_python_constants_match_the_header(api):
     """The binding mirrors the header's constants by hand; they must agree."""
     h = _header_constants()
     for name in ("ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
-                 "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_F32", "ATTN_BF16"):
+                 "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_ERR_BOUNDS", "ATTN_F32",
+                 "ATTN_BF16"):
         assert getattr(api, name) == h[name], name
     assert api.NOALLOC_SCRATCH_BYTES == h["ATTN_NOALLOC_SCRATCH_BYTES"]
     ids = {"K_FWD": "ATTN_PROFILE_FWD", "K_BWD_PRE": "ATTN_PROFILE_BWD_PRE", "K_BWD_MAIN": "ATTN_PROFILE_BWD_MAIN",
@@ -75,7 +76,7 @@ def test_python_constants_match_the_header(api):
 
 
 def test_status_strings(api):
-    for s in range(7):
+    for s in range(8):
         assert api.attn_status_string(s).startswith("ATTN_")
     assert "UNKNOWN" in api.attn_status_string(99)
 
