@@ -262,7 +262,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
   int* gerr = p.err;
   pdl_launch_and_wait();
 
-  if (warp >= 12) {
+  if (warp >= 8) {
     setmaxnreg_dec<REG_OTHER>();
     if (warp == 12) {
       // ------------------------------------------------------------ loader: K, Q, dO
@@ -385,10 +385,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
         }
         if (ok && have_pend) ok = finish(pend);
       }
-    }
-  } else if (warp >= 8) {
-    setmaxnreg_dec<REG_OTHER>();  // own branch: the compiler allocates this role apart
-    {
+    } else if (warp < 12) {
       // ------------------------------------------------------------ dQ warpgroup
       const int wq = warp - 8;
       const int r = (wq << 5) + lane;                // query row (dQ) / key row (dK, dV)
@@ -438,20 +435,31 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
         }
         if (!ok) break;
         // ---------------------------------------------------------- dK, dV of this item
-        // dV and scale*dK go to registers (bf16 pairs) first and the TMEM
-        // columns are handed back to the next item's first dK and dV at once;
-        // the staging tile (still read by the last dQ reduction) and the
-        // stores come after.
+        // dV goes to the staging tile and scale*dK to registers (bf16 pairs)
+        // before either is stored, so the TMEM columns are handed back to the
+        // next item's first dK and dV without waiting for the stores.
         const bool fail = !mbar_wait(&bar_done, ic & 1, &abort_sh, gerr);
         tc_fence_after();
-        uint32_t dvp[HS / 2], dkp[HS / 2];
+        if (leader) bulk_wait_group_read0();             // staging free
+        if (named_bar_red_or(1, 128, fail)) { ok = false; break; }
+        uint8_t* stage = sdq;
 #pragma unroll
         for (int cc = 0; cc < HS; cc += 16) {
           uint32_t o[16];
           tmem_ld16_wait(tmem + lane_off + TB_DV + cc, o);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) dvp[cc / 2 + e] = pack_bf16x2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
+          uint4 v0, v1;
+          v0.x = pack_bf16x2(__uint_as_float(o[0]), __uint_as_float(o[1]));
+          v0.y = pack_bf16x2(__uint_as_float(o[2]), __uint_as_float(o[3]));
+          v0.z = pack_bf16x2(__uint_as_float(o[4]), __uint_as_float(o[5]));
+          v0.w = pack_bf16x2(__uint_as_float(o[6]), __uint_as_float(o[7]));
+          v1.x = pack_bf16x2(__uint_as_float(o[8]), __uint_as_float(o[9]));
+          v1.y = pack_bf16x2(__uint_as_float(o[10]), __uint_as_float(o[11]));
+          v1.z = pack_bf16x2(__uint_as_float(o[12]), __uint_as_float(o[13]));
+          v1.w = pack_bf16x2(__uint_as_float(o[14]), __uint_as_float(o[15]));
+          *reinterpret_cast<uint4*>(stage + swz_chunk_offset<HS>(r, cc / 8)) = v0;
+          *reinterpret_cast<uint4*>(stage + swz_chunk_offset<HS>(r, cc / 8 + 1)) = v1;
         }
+        uint32_t dkp[HS / 2];
 #pragma unroll
         for (int cc = 0; cc < HS; cc += 16) {
           uint32_t o[16];
@@ -464,13 +472,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_consta
         // every commit is awaited: only signal if the MMA warp will wait for it
         __syncwarp();
         if (lane == 0 && ic + 1 < n_items_cta) mbar_arrive(&bar_epi_free);   // dK/dV TMEM columns free
-        if (leader) bulk_wait_group_read0();             // staging free
-        if (named_bar_red_or(1, 128, fail)) { ok = false; break; }
-        uint8_t* stage = sdq;
-#pragma unroll
-        for (int ch = 0; ch < HS / 8; ++ch)
-          *reinterpret_cast<uint4*>(stage + swz_chunk_offset<HS>(r, ch)) =
-              make_uint4(dvp[ch * 4 + 0], dvp[ch * 4 + 1], dvp[ch * 4 + 2], dvp[ch * 4 + 3]);
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (leader) {
