@@ -18,10 +18,11 @@
 //      b, h); a CTA walks its items (causal items dealt longest first, each to
 //      the CTA with the least work so far, as the forward's; otherwise in a
 //      snake order over the CTAs) and, per item, the query tiles that see
-//      those keys. S^T, dP^T, dV, dK, dQ on tcgen05; dQ tiles are added into
+//      those keys. S, dP, dV, dK, dQ on tcgen05; dQ tiles are added into
 //      the accumulator with TMA bulk reductions; dK/dV stored by TMA.
-//      K/V are double-buffered and the Q/dO ring runs on across items, so the
-//      next item's loads and the last item's dK/dV stores overlap compute.
+//      K is double-buffered, V refilled once an item's last dP is done, and
+//      the Q/dO ring runs on across items, so the next item's loads and the
+//      last item's dK/dV stores overlap compute.
 //   3. attn_bwd_dq_out: dq accumulator -> bf16 into dqkv[:, :, 0:C].
 //
 // Main kernel: 16 warps.
