@@ -23,6 +23,9 @@
 //   (setmaxnreg: 208 registers for the softmax warpgroups, 80 for warps 8-11)
 // S_i(j+1) is issued as soon as the softmax warps of tile i hold S_i(j) in
 // registers, so the next scores are ready when the softmax of this tile ends.
+// The two softmax warpgroups take turns at the exponentials (two named
+// barriers), so one forms P while the other loads its scores and takes its
+// row maxima, instead of both sharing the MUFU at once.
 // Each warpgroup writes its output tile through its own (then dead) Q tile and
 // a TMA store while the next item's first scores are computed.
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+HS) O1 [320,320+HS)
@@ -250,6 +253,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
     const uint32_t tO = tmem + lane_off + (wg ? TM_O1 : TM_O0);
     const uint32_t tP = tmem + lane_off + (wg ? TM_P1 : TM_P0);
     const uint32_t bar_id = 1 + wg;              // named barrier of this warpgroup
+    // The two warpgroups take turns at the exponentials (named barriers 3 and
+    // 4, 256 threads), tile 1 first at every key step: one forms P while the
+    // other waits for its scores and takes its row maxima, so the two tiles'
+    // exponentials do not share the MUFU. Every warp takes one turn per key
+    // step of every item (with no work where its tile has no such step or its
+    // wait gave up), so the hand-overs always pair up. Tile 0's causal rows
+    // end one key tile earlier; its spare turn follows tile 1's last step, so
+    // tile 1 starts the next item without waiting for tile 0.
+    const uint32_t my_turn = 3 + wg, next_turn = 4 - wg;
+    auto idle_turns = [&](int k) {
+      for (; k > 0; --k) {
+        named_bar_sync(my_turn, 256);
+        named_bar_arrive(next_turn, 256);
+      }
+    };
     const bool leader = (warp & 3) == 0 && lane == 0;
     const float c = p.scale_log2;
     bool ok = true;
@@ -262,14 +280,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
       }
       q_pending = -1;
     };
+    if (wg == 0) named_bar_arrive(4, 256);       // tile 1 takes the first turn
     FwdItem w_next = n_items_cta > 0 ? fwd_decode<CAUSAL>(deal_item(sched, 0), p) : FwdItem{};
-    for (int ic = 0; ok && ic < n_items_cta; ++ic) {
+    int ic = 0;
+    for (; ok && ic < n_items_cta; ++ic) {
       const FwdItem w = w_next;                  // decoded one item ahead
       if (ic + 1 < n_items_cta) w_next = fwd_decode<CAUSAL>(deal_item(sched, ic + 1), p);
       const int qb = ic & 1;
       const int n = w.n_tile[wg];
       const int t = w.q0 + wg * BM + r;          // query row
       float m_run = -INFINITY, l_run = 0.f;
+      int turns = 0;                             // turns taken in this item
       for (int j = 0; j < n; ++j) {
         const int gj = gs + j;
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[wg], gj & 1, &abort_sh, gerr));
@@ -316,6 +337,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
         const float alpha = ex2_approx((m_run - m_new) * c);
         const float2 c2 = make_float2(c, c), nmc = make_float2(-m_new * c, -m_new * c);
         float2 ls[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+        named_bar_sync(my_turn, 256);                    // this warpgroup's turn
         // p = exp2(s*c - m*c) in packed pairs; P goes to TMEM in two 64-key halves
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -350,6 +372,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
           }
           tmem_st32(tP + hf * 32, pk);
         }
+        named_bar_arrive(next_turn, 256);                // the other warpgroup's turn
+        ++turns;
         if (!ok) break;
         const float lsum = ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
         l_run = l_run * alpha + lsum;
@@ -360,6 +384,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
         if (lane == 0) mbar_arrive(&bar_p[wg]);
         if (j == 0) release_q();
       }
+      idle_turns(w.n_max - turns);
       // -------------------------------------------------------- epilogue of this item
       // A warp whose wait gave up left the key loop early, but it still comes
       // here: failures are combined over the warpgroup at the barrier below, so
@@ -400,6 +425,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv,
       if (ic + 2 < n_items_cta) q_pending = qb;
       gs += n;
     }
+    // after a failure: the turns of the items not walked (the failed item's
+    // were all taken before its epilogue)
+    for (++ic; ic < n_items_cta; ++ic) idle_turns(fwd_decode<CAUSAL>(deal_item(sched, ic), p).n_max);
+    if (wg == 1) named_bar_sync(4, 256);         // the other warpgroup's last hand-over
     if (leader) bulk_wait_group0();
   }
 

@@ -66,6 +66,12 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrive at named barrier `id` without waiting (its other `nthreads` minus
+// these threads wait there with named_bar_sync).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
 // Named barrier that also ORs a predicate over the participating threads, so
 // a failure seen by any thread becomes a decision every thread shares.
 __device__ __forceinline__ bool named_bar_red_or(uint32_t id, uint32_t nthreads, bool pred) {
