@@ -42,8 +42,9 @@ cudaError_t launch_att(const CUtensorMap& map_qkv, const CUtensorMap& map_pre, c
 size_t decode_workspace_bytes(int B, int L, int C, int NH, int Tq, bool f32);
 int decode_max_tq();
 int decode_chunk(bool f32);
-cudaError_t launch_decode(const CUtensorMap& map_qkv, const void* qkv, void* out, float* lse, float* part, bool f32,
-                          int B, int L, int C, int NH, int Tq, cudaStream_t stream);
+cudaError_t launch_decode(const CUtensorMap& map_qkv, const CUtensorMap& map_kq, const CUtensorMap& map_q,
+                          const void* qkv, void* out, float* lse, float* part, bool f32, int B, int L, int C, int NH,
+                          int Tq, cudaStream_t stream);
 
 static __device__ int g_error_word = 0;
 
@@ -501,11 +502,20 @@ extern "C" attn_status_t attn_decode(const void* qkv, void* out, float* lse, int
     return ATTN_ERR_INVALID_ARG;
   if (!device_error_word()) return ATTN_ERR_CUDA;
   const bool f32 = dtype == ATTN_F32;
-  CUtensorMap mq;
+  CUtensorMap mq, mkq, mqs;
   if (!encode_3d(&mq, qkv, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 ? 4 : 2,
                  3 * C, L, B, C / NH, decode_chunk(f32), CU_TENSOR_MAP_SWIZZLE_NONE))
     return ATTN_ERR_CUDA;
-  cudaError_t ce = launch_decode(mq, qkv, out, lse, static_cast<float*>(workspace), f32, B, L, C, NH, Tq,
+  mkq = mq;
+  mqs = mq;
+  if (!f32) {
+    // K and the query rows for the tensor-core scores, in the hs-row swizzle
+    const CUtensorMapSwizzle swz = C / NH == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!encode_3d(&mkq, qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3 * C, L, B, C / NH, decode_chunk(false), swz) ||
+        !encode_3d(&mqs, qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 3 * C, L, B, C / NH, 16, swz))
+      return ATTN_ERR_CUDA;
+  }
+  cudaError_t ce = launch_decode(mq, mkq, mqs, qkv, out, lse, static_cast<float*>(workspace), f32, B, L, C, NH, Tq,
                                  static_cast<cudaStream_t>(stream));
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

@@ -22,8 +22,8 @@
 //                       chunk-local softmax (max, exp2, sum); the partial
 //                       output summed over the rows of a warp and the warps;
 //                       written as (m, l, o)
-//   attn_decode_combine one warp-pair per (b, h, i): merges the chunks'
-//                       partial results (log-sum-exp rescaling) into out, lse
+//   attn_decode_combine one warp per (b, h, i): merges the chunks' partial
+//                       results (log-sum-exp rescaling) into out, lse
 #include "../../include/attn.h"
 #include "common.cuh"
 
@@ -109,9 +109,28 @@ __host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x
 // TQ: the largest Tq this instantiation serves (1, 4 or 8); its per-query
 // shared arrays and accumulators are sized by it, so the common one-token step
 // keeps more CTAs resident per SM.
+// With bf16 inputs and several query tokens the scores come from the tensor
+// core: S^T = K Q^T for the chunk's 128 keys (TMEM lanes) and the queries
+// padded to 16 (columns), one tcgen05 group of hs/16 instructions, read back
+// one key row per thread; K and the queries arrive by swizzled tensor copies
+// (map_kq: box {hs, 128 rows}, map_q: box {hs, 16 rows}). One query token,
+// or fp32 inputs, keep the scores on the FMA pipe (exact fp32 products).
+template <typename E, int HS, int TQ>
+struct DecodeMma {
+  static constexpr bool on = sizeof(E) == 2 && TQ > 1;
+};
+template <typename E, int HS, int TQ>
+__host__ __device__ constexpr int split_smem_bytes() {
+  return DecodeMma<E, HS, TQ>::on ? 2 * Chunk<E>::N * HS * (int)sizeof(E) + 16 * HS * 2 + 1024
+                                  : 2 * Chunk<E>::N * HS * (int)sizeof(E) + 128;
+}
+
 template <typename E, int HS, int TQ>
 __global__ void __launch_bounds__(THREADS)
-attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
+attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_kq,
+                  const __grid_constant__ CUtensorMap map_q, const Params p) {
+  constexpr bool MMA = DecodeMma<E, HS, TQ>::on;
+  static_assert(!MMA || THREADS == Chunk<E>::N, "tensor-core scores: one thread per key of the chunk");
   // A K or V row (HS elements) is read by LPR lanes, 8 elements each, so a
   // warp instruction covers whole rows; GROUPS rows at a time.
   constexpr int CH = Chunk<E>::N;
@@ -127,13 +146,17 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
   constexpr int O_OUT = (8 * TQ) >> O_LEVELS;
   static_assert(O_OUT >= 1, "output reduction leaves at least one value per lane");
   extern __shared__ uint8_t smem_raw[];
-  E* sK = reinterpret_cast<E*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  // the tensor core reads swizzled K and Q tiles from 1024-byte aligned starts
+  constexpr uintptr_t ALIGN = MMA ? 1023 : 127;
+  E* sK = reinterpret_cast<E*>((reinterpret_cast<uintptr_t>(smem_raw) + ALIGN) & ~ALIGN);
   E* sV = sK + CH * HS;
+  E* sQ = sV + CH * HS;                         // MMA path: 16 query rows
   __shared__ float sp[TQ][CH];
   __shared__ float red[TQ][THREADS / 32];
   __shared__ float row_m[TQ];
   __shared__ float sacc[THREADS / 32][TQ][HS];
-  __shared__ uint64_t bar_k, bar_v;
+  __shared__ uint64_t bar_k, bar_v, bar_s;
+  __shared__ uint32_t tmem_sh;
   __shared__ volatile int abort_sh;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -153,15 +176,29 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
     abort_sh = 0;
     mbar_init(&bar_k, 1);
     mbar_init(&bar_v, 1);
+    mbar_init(&bar_s, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar_k, BYTES);
-    tma_load_3d(sK, &map_qkv, &bar_k, C + h * HS, j0, b);
+    if constexpr (MMA) {
+      // K (swizzled) and the 16 rows from the first query on (rows past L read as zero)
+      mbar_arrive_expect_tx(&bar_k, BYTES + 16 * HS * 2);
+      tma_load_3d(sK, &map_kq, &bar_k, C + h * HS, j0, b);
+      tma_load_3d(sQ, &map_q, &bar_k, h * HS, L - Tq, b);
+    } else {
+      mbar_arrive_expect_tx(&bar_k, BYTES);
+      tma_load_3d(sK, &map_qkv, &bar_k, C + h * HS, j0, b);
+    }
     mbar_arrive_expect_tx(&bar_v, BYTES);
     tma_load_3d(sV, &map_qkv, &bar_v, 2 * C + h * HS, j0, b);
   }
+  if constexpr (MMA) {
+    if (warp == 0) {
+      tmem_alloc(&tmem_sh, 32);
+      tmem_relinquish();
+    }
+  }
   // this lane's 8 columns of the queries (the last Tq positions), in registers
-  float2 qr[TQ][4];
-  {
+  float2 qr[MMA ? 1 : TQ][4];
+  if constexpr (!MMA) {
     const size_t rs = (size_t)3 * C;
     const E* qbase = static_cast<const E*>(p.qkv) + (size_t)b * L * rs + h * HS + db;
 #pragma unroll
@@ -172,8 +209,43 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
       for (int k = 0; k < 4; ++k) qr[i][k] = make_float2(v[2 * k], v[2 * k + 1]);
     }
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
   bool ok = mbar_wait(&bar_k, 0, &abort_sh, p.err);
+  if constexpr (MMA) {
+    using G = TileGeom<HS>;
+    const uint32_t tmem = tmem_sh;
+    if (tid == 0 && ok) {
+      tc_fence_after();
+      const uint64_t dk = make_sdesc(smem_u32(sK), 16, G::ATOM_BYTES, G::SWZ);
+      const uint64_t dq = make_sdesc(smem_u32(sQ), 16, G::ATOM_BYTES, G::SWZ);
+      constexpr uint32_t idesc = make_idesc_bf16(CH, 16, false, false);
+#pragma unroll
+      for (int k = 0; k < HS / 16; ++k) mma_ss(tmem, desc_add(dk, k * 32), desc_add(dq, k * 32), idesc, k > 0);
+      mma_commit(&bar_s);
+    }
+    ok = mbar_wait(&bar_s, 0, &abort_sh, p.err) && ok;
+    if (ok) {
+      tc_fence_after();
+      uint32_t sc[16];
+      tmem_ld16_wait(tmem + ((uint32_t)(warp * 32) << 16), sc);
+      const int j = tid;                              // key of this thread = TMEM lane
+#pragma unroll
+      for (int i = 0; i < TQ; ++i)
+        if (i < Tq)
+          sp[i][j] = (j < nk && j0 + j <= L - Tq + i) ? __uint_as_float(sc[i]) * p.scale_log2 : -INFINITY;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      // a wait that gave up may leave the group in flight: let it land first
+      if (abort_sh)
+        for (int k = 0; k < 1000; ++k) __nanosleep(1000);
+      __syncwarp();
+      tmem_dealloc(tmem, 32);
+    }
+  } else
   // scores: packed partial dot products over the lane's 8 columns, then the
   // transposing butterfly over the row's lanes
   for (int r0 = 0; r0 < CH; r0 += GROUPS) {
@@ -290,45 +362,83 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const Params p) {
   }
 }
 
-// One block of HS threads per (b, h, query): merge the chunks' partials.
+// One warp per (b, h, query), four per block: merge the chunks' partials.
+// The chunk maxima and row sums are read one chunk per lane; the outputs,
+// HS/32 columns per lane, with four chunks' loads in flight at a time.
+constexpr int COMBINE_WARPS = 4;
 template <typename E, int HS>
-__global__ void __launch_bounds__(HS) attn_decode_combine(const Params p) {
-  const int i = blockIdx.x % p.Tq;
-  const int bh = blockIdx.x / p.Tq;
-  const int b = bh / p.NH, h = bh % p.NH;
-  const int d = threadIdx.x;
+__global__ void __launch_bounds__(32 * COMBINE_WARPS) attn_decode_combine(const Params p) {
+  constexpr int DPL = HS / 32;                       // output columns per lane
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * COMBINE_WARPS + (threadIdx.x >> 5);
   const int Tq = p.Tq;
+  if (gw >= p.BH * Tq) return;
+  const int i = gw % Tq, bh = gw / Tq;
+  const int b = bh / p.NH, h = bh % p.NH;
   // only chunks that hold a visible key of this query contribute
-  const int last = (p.L - Tq + i) / Chunk<E>::N;
-  if (!ATTN_IN_RANGE(bh < p.BH && last < p.n_split && d < HS, p.err)) return;
-  const float* rec = p.part + (size_t)bh * p.n_split * Tq * (HS + 2) + i * (HS + 2);
+  const int n = (p.L - Tq + i) / Chunk<E>::N + 1;
+  if (!ATTN_IN_RANGE(n <= p.n_split, p.err)) return;
+  const size_t stride = (size_t)Tq * (HS + 2);       // floats between two chunks' records
+  const float* rec = p.part + (size_t)bh * p.n_split * stride + (size_t)i * (HS + 2);
   float M = -INFINITY;
-  for (int s = 0; s <= last; ++s) M = fmaxf(M, rec[(size_t)s * Tq * (HS + 2)]);
-  float l = 0.f, o = 0.f;
-  for (int s = 0; s <= last; ++s) {
-    const float* r = rec + (size_t)s * Tq * (HS + 2);
-    const float w = ex2_approx(r[0] - M);
-    l = fmaf(r[1], w, l);
-    o = fmaf(r[2 + d], w, o);
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, rec[s * stride]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float l = 0.f;
+  for (int s = lane; s < n; s += 32) l = fmaf(rec[s * stride + 1], ex2_approx(rec[s * stride] - M), l);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  float acc[DPL];
+#pragma unroll
+  for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
+  int s = 0;
+  for (; s + 4 <= n; s += 4) {
+    float w[4], v[4][DPL];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float* r = rec + (s + u) * stride;
+      w[u] = r[0];
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) v[u][k] = r[2 + k * 32 + lane];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float wu = ex2_approx(w[u] - M);
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) acc[k] = fmaf(v[u][k], wu, acc[k]);
+    }
   }
-  const float val = o / l;
-  const size_t oi = ((size_t)b * Tq + i) * p.C + h * HS + d;
-  if constexpr (sizeof(E) == 4) static_cast<float*>(p.out)[oi] = val;
-  else static_cast<uint16_t*>(p.out)[oi] = (uint16_t)(pack_bf16x2(val, 0.f) & 0xFFFFu);
-  if (d == 0) p.lse[(size_t)bh * Tq + i] = (M + __log2f(l)) * 0.69314718055994531f;
+  for (; s < n; ++s) {
+    const float* r = rec + s * stride;
+    const float wu = ex2_approx(r[0] - M);
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) acc[k] = fmaf(r[2 + k * 32 + lane], wu, acc[k]);
+  }
+  const float inv_l = 1.f / l;
+#pragma unroll
+  for (int k = 0; k < DPL; ++k) {
+    const float val = acc[k] * inv_l;
+    const size_t oi = ((size_t)b * Tq + i) * p.C + h * HS + k * 32 + lane;
+    if constexpr (sizeof(E) == 4) static_cast<float*>(p.out)[oi] = val;
+    else static_cast<uint16_t*>(p.out)[oi] = (uint16_t)(pack_bf16x2(val, 0.f) & 0xFFFFu);
+  }
+  if (lane == 0) p.lse[(size_t)bh * Tq + i] = (M + __log2f(l)) * 0.69314718055994531f;
 }
 
 template <typename E, int HS>
-static cudaError_t launch_t(const CUtensorMap& m, const Params& p, int BH, cudaStream_t s) {
-  constexpr int SMEM = 2 * Chunk<E>::N * HS * (int)sizeof(E) + 128;
+static cudaError_t launch_t(const CUtensorMap& m, const CUtensorMap& mkq, const CUtensorMap& mq, const Params& p,
+                            int BH, cudaStream_t s) {
   auto k = p.Tq == 1 ? attn_decode_split<E, HS, 1>
                      : (p.Tq <= 4 ? attn_decode_split<E, HS, 4> : attn_decode_split<E, HS, MAX_TQ>);
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  const int smem = p.Tq == 1 ? split_smem_bytes<E, HS, 1>()
+                             : (p.Tq <= 4 ? split_smem_bytes<E, HS, 4>() : split_smem_bytes<E, HS, MAX_TQ>());
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<(unsigned)(BH * p.n_split), THREADS, SMEM, s>>>(m, p);
+  k<<<(unsigned)(BH * p.n_split), THREADS, smem, s>>>(m, mkq, mq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_decode_combine<E, HS><<<(unsigned)(BH * p.Tq), HS, 0, s>>>(p);
+  attn_decode_combine<E, HS><<<(unsigned)((BH * p.Tq + COMBINE_WARPS - 1) / COMBINE_WARPS), 32 * COMBINE_WARPS, 0,
+                                 s>>>(p);
   return cudaGetLastError();
 }
 
@@ -344,9 +454,12 @@ size_t decode_workspace_bytes(int B, int L, int C, int NH, int Tq, bool f32) {
 
 int decode_max_tq() { return deck::MAX_TQ; }
 
-// map_qkv: qkv as {3C, L, B}, box {hs, chunk rows, 1}, no swizzle
-cudaError_t launch_decode(const CUtensorMap& map_qkv, const void* qkv, void* out, float* lse, float* part, bool f32,
-                          int B, int L, int C, int NH, int Tq, cudaStream_t stream) {
+// map_qkv: qkv as {3C, L, B}, box {hs, chunk rows, 1}, no swizzle; map_kq and
+// map_q: the same tensor in the hs-row swizzle (128 bytes for hs 64, 64 for
+// hs 32), boxes {hs, 128, 1} and {hs, 16, 1} (bf16 only; unused for fp32)
+cudaError_t launch_decode(const CUtensorMap& map_qkv, const CUtensorMap& map_kq, const CUtensorMap& map_q,
+                          const void* qkv, void* out, float* lse, float* part, bool f32, int B, int L, int C, int NH,
+                          int Tq, cudaStream_t stream) {
   deck::Params p;
   p.qkv = qkv;
   p.out = out;
@@ -363,9 +476,10 @@ cudaError_t launch_decode(const CUtensorMap& map_qkv, const void* qkv, void* out
   p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)hs));
   const int BH = B * NH;
   if (f32)
-    return hs == 64 ? deck::launch_t<float, 64>(map_qkv, p, BH, stream) : deck::launch_t<float, 32>(map_qkv, p, BH, stream);
-  return hs == 64 ? deck::launch_t<uint16_t, 64>(map_qkv, p, BH, stream)
-                  : deck::launch_t<uint16_t, 32>(map_qkv, p, BH, stream);
+    return hs == 64 ? deck::launch_t<float, 64>(map_qkv, map_kq, map_q, p, BH, stream)
+                    : deck::launch_t<float, 32>(map_qkv, map_kq, map_q, p, BH, stream);
+  return hs == 64 ? deck::launch_t<uint16_t, 64>(map_qkv, map_kq, map_q, p, BH, stream)
+                  : deck::launch_t<uint16_t, 32>(map_qkv, map_kq, map_q, p, BH, stream);
 }
 
 }  // namespace attn
