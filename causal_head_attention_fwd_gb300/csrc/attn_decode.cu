@@ -109,19 +109,27 @@ __host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x
 // TQ: the largest Tq this instantiation serves (1, 4 or 8); its per-query
 // shared arrays and accumulators are sized by it, so the common one-token step
 // keeps more CTAs resident per SM.
-// With bf16 inputs and several query tokens the scores come from the tensor
-// core: S^T = K Q^T for the chunk's 128 keys (TMEM lanes) and the queries
+// With bf16 inputs and several query tokens both products run on the tensor
+// core. S^T = K Q^T for the chunk's 128 keys (TMEM lanes) and the queries
 // padded to 16 (columns), one tcgen05 group of hs/16 instructions, read back
-// one key row per thread; K and the queries arrive by swizzled tensor copies
-// (map_kq: box {hs, 128 rows}, map_q: box {hs, 16 rows}). One query token,
-// or fp32 inputs, keep the scores on the FMA pipe (exact fp32 products).
+// one key row per thread. The exponentials go to shared memory as bf16 P,
+// rows = queries, K-major in the 128-byte swizzle (16 rows of each 64-key
+// half are written; the rows past them that the M = 128 product reads are
+// other data, and only output rows below Tq are used), and O = P V is a
+// second group (N = hs, 8 instructions, over the columns S^T held) whose
+// rows warp 0 reads from TMEM. 64 TMEM columns per CTA.
+// K, V and the queries arrive by swizzled tensor copies (map_kq: box
+// {hs, 128 rows}, map_q: box {hs, 16 rows}). One query token, or fp32 inputs,
+// keep both products on the FMA pipe (exact fp32 products).
 template <typename E, int HS, int TQ>
 struct DecodeMma {
   static constexpr bool on = sizeof(E) == 2 && TQ > 1;
 };
+constexpr int P_TILE_BYTES = 2 * 16 * 128;      // P: 2 key halves x 16 query rows x 128 bytes
+constexpr int TMEM_COLS = 64;                   // S^T (16 columns), then O over them (hs columns)
 template <typename E, int HS, int TQ>
 __host__ __device__ constexpr int split_smem_bytes() {
-  return DecodeMma<E, HS, TQ>::on ? 2 * Chunk<E>::N * HS * (int)sizeof(E) + 16 * HS * 2 + 1024
+  return DecodeMma<E, HS, TQ>::on ? P_TILE_BYTES + 2 * Chunk<E>::N * HS * (int)sizeof(E) + 16 * HS * 2 + 1024
                                   : 2 * Chunk<E>::N * HS * (int)sizeof(E) + 128;
 }
 
@@ -146,16 +154,19 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
   constexpr int O_OUT = (8 * TQ) >> O_LEVELS;
   static_assert(O_OUT >= 1, "output reduction leaves at least one value per lane");
   extern __shared__ uint8_t smem_raw[];
-  // the tensor core reads swizzled K and Q tiles from 1024-byte aligned starts
+  // the tensor core reads swizzled tiles from 1024-byte aligned starts; P
+  // comes first, so its M = 128 operand reads stay inside the allocation
   constexpr uintptr_t ALIGN = MMA ? 1023 : 127;
-  E* sK = reinterpret_cast<E*>((reinterpret_cast<uintptr_t>(smem_raw) + ALIGN) & ~ALIGN);
+  uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + ALIGN) & ~ALIGN);
+  uint8_t* sP = sbase;                          // MMA path only
+  E* sK = reinterpret_cast<E*>(sbase + (MMA ? P_TILE_BYTES : 0));
   E* sV = sK + CH * HS;
   E* sQ = sV + CH * HS;                         // MMA path: 16 query rows
   __shared__ float sp[TQ][CH];
   __shared__ float red[TQ][THREADS / 32];
   __shared__ float row_m[TQ];
-  __shared__ float sacc[THREADS / 32][TQ][HS];
-  __shared__ uint64_t bar_k, bar_v, bar_s;
+  __shared__ float sacc[MMA ? 1 : THREADS / 32][MMA ? 1 : TQ][MMA ? 1 : HS];
+  __shared__ uint64_t bar_k, bar_v, bar_s, bar_o;
   __shared__ uint32_t tmem_sh;
   __shared__ volatile int abort_sh;
 
@@ -177,6 +188,7 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
     mbar_init(&bar_k, 1);
     mbar_init(&bar_v, 1);
     mbar_init(&bar_s, 1);
+    mbar_init(&bar_o, 1);
     fence_mbar_init();
     if constexpr (MMA) {
       // K (swizzled) and the 16 rows from the first query on (rows past L read as zero)
@@ -188,11 +200,11 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
       tma_load_3d(sK, &map_qkv, &bar_k, C + h * HS, j0, b);
     }
     mbar_arrive_expect_tx(&bar_v, BYTES);
-    tma_load_3d(sV, &map_qkv, &bar_v, 2 * C + h * HS, j0, b);
+    tma_load_3d(sV, MMA ? &map_kq : &map_qkv, &bar_v, 2 * C + h * HS, j0, b);
   }
   if constexpr (MMA) {
     if (warp == 0) {
-      tmem_alloc(&tmem_sh, 32);
+      tmem_alloc(&tmem_sh, TMEM_COLS);
       tmem_relinquish();
     }
   }
@@ -213,9 +225,9 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
   __syncthreads();
   tc_fence_after();
   bool ok = mbar_wait(&bar_k, 0, &abort_sh, p.err);
+  using G = TileGeom<HS>;
+  const uint32_t tmem = MMA ? tmem_sh : 0u;
   if constexpr (MMA) {
-    using G = TileGeom<HS>;
-    const uint32_t tmem = tmem_sh;
     if (tid == 0 && ok) {
       tc_fence_after();
       const uint64_t dk = make_sdesc(smem_u32(sK), 16, G::ATOM_BYTES, G::SWZ);
@@ -236,15 +248,7 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
         if (i < Tq)
           sp[i][j] = (j < nk && j0 + j <= L - Tq + i) ? __uint_as_float(sc[i]) * p.scale_log2 : -INFINITY;
     }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-      // a wait that gave up may leave the group in flight: let it land first
-      if (abort_sh)
-        for (int k = 0; k < 1000; ++k) __nanosleep(1000);
-      __syncwarp();
-      tmem_dealloc(tmem, 32);
-    }
+    tc_fence_before();                              // S^T read: O may overwrite its columns
   } else
   // scores: packed partial dot products over the lane's 8 columns, then the
   // transposing butterfly over the row's lanes
@@ -293,15 +297,72 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
     float l = 0.f;
     for (int j = tid; j < CH; j += THREADS) {
       const float e = m == -INFINITY ? 0.f : ex2_approx(sp[i][j] - m);
-      sp[i][j] = e;
+      if constexpr (MMA) {
+        // P[i][j] (bf16) at row i of key half j/64, chunk (j%64)/8 swizzled by row
+        const int kk = j & 63;
+        *reinterpret_cast<uint16_t*>(sP + (j >> 6) * (16 * 128) + i * 128 + ((((kk >> 3) ^ (i & 7)) << 4)) +
+                                     (kk & 7) * 2) = (uint16_t)(pack_bf16x2(e, 0.f) & 0xFFFFu);
+      } else {
+        sp[i][j] = e;
+      }
       l += e;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     if (lane == 0) red[i][warp] = l;
   }
+  if constexpr (MMA) fence_proxy_async_smem();     // P is read by the tensor core
   __syncthreads();
   ok = mbar_wait(&bar_v, 0, &abort_sh, p.err) && ok;
+  if constexpr (MMA) {
+    // O = P V: A = P (K-major, the second key half 2 KB on), B = V (MN-major)
+    if (tid == 0 && ok) {
+      tc_fence_after();
+      const uint64_t dp = make_sdesc(smem_u32(sP), 16, 1024, SWZ_128B);
+      const uint64_t dv = make_sdesc(smem_u32(sV), 16, G::ATOM_BYTES, G::SWZ);
+      constexpr uint32_t idesc = make_idesc_bf16(CH, HS, false, true);
+#pragma unroll
+      for (int k = 0; k < CH / 16; ++k)
+        mma_ss(tmem, desc_add(dp, (k >> 2) * (16 * 128) + (k & 3) * 32),
+               desc_add(dv, k * 16 * G::ROW_BYTES), idesc, k > 0);
+      mma_commit(&bar_o);
+    }
+    ok = mbar_wait(&bar_o, 0, &abort_sh, p.err) && ok;
+    if (warp == 0 && ok) {
+      // query rows = TMEM lanes 0..Tq-1: m (log2 units), l, o[HS]
+      tc_fence_after();
+      uint32_t o[HS];
+#pragma unroll
+      for (int c0 = 0; c0 < HS; c0 += 16) {
+        uint32_t t16[16];
+        tmem_ld16_wait(tmem + c0, t16);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) o[c0 + k] = t16[k];
+      }
+      if (lane < Tq) {
+        float* rec = p.part + (((size_t)bh * p.n_split + split) * Tq + lane) * (HS + 2);
+        float l = 0.f;
+#pragma unroll
+        for (int w = 0; w < THREADS / 32; ++w) l += red[lane][w];
+        rec[0] = row_m[lane];
+        rec[1] = l;
+        // records are HS + 2 floats long: 8-byte aligned, so pairs
+#pragma unroll
+        for (int d = 0; d < HS; d += 2)
+          *reinterpret_cast<float2*>(rec + 2 + d) = make_float2(__uint_as_float(o[d]), __uint_as_float(o[d + 1]));
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      // a wait that gave up may leave a group in flight: let it land first
+      if (abort_sh)
+        for (int k = 0; k < 1000; ++k) __nanosleep(1000);
+      __syncwarp();
+      tmem_dealloc(tmem, TMEM_COLS);
+    }
+    return;
+  }
   // partial outputs: each lane accumulates its 8 columns over its rows of the
   // chunk for every query (packed pairs), then the transposing butterfly sums
   // the rows of the warp and the warps are summed through shared memory
