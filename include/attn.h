@@ -180,7 +180,9 @@ attn_status_t attn_fwd_att(const void* qkv, const float* lse, float* preatt, flo
  *   workspace : attn_decode_workspace_size(...) bytes, 256-byte aligned,
  *               owned by the caller (per-chunk partial results).
  * 1 <= Tq <= min(L, 8); hs in {32, 64}. A stream over the cache, bound by HBM
- * bandwidth; runs on the CUDA cores (fp32 arithmetic), not the tensor core.
+ * bandwidth. One query token, or fp32 inputs: CUDA cores, fp32 arithmetic.
+ * bf16 inputs with Tq > 1: both products on the tensor core (bf16 operands,
+ * P rounded to bf16 as in attn_fwd, fp32 accumulation).
  */
 size_t attn_decode_workspace_size(int B, int L, int C, int NH, int Tq, attn_dtype_t dtype);
 attn_status_t attn_decode(const void* qkv, void* out, float* lse, int B, int L, int C, int NH, int Tq,
