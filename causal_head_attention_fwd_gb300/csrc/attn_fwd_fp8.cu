@@ -21,7 +21,8 @@
 // "Umakini wa kujitegemea, kerneli za CUDA na FlashAttention" section 3):
 // persistent CTAs, work item = two 128-row query tiles of one (b, h), items
 // dealt longest first as in fwd_deal.cuh, 12 warps
-//   warps 0-3 / 4-7  softmax warpgroups of query tiles 0 / 1 (TMEM lanes)
+//   warps 0-3 / 4-7  softmax warpgroups of query tiles 0 / 1 (TMEM lanes);
+//                    non-causal: taking turns at the exponentials
 //   warp  8          TMA producer (Q per item, K/V through a ring)
 //   warps 9-10       MMA issuers, one per query tile; warp 11 idle
 // Tiles: [128 rows][hs] e4m3, hs bytes per row (64- or 32-byte swizzle). S and
@@ -280,12 +281,28 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
     const uint32_t tO = tmem + lane_off + (wg ? TM_O1 : TM_O0);
     const uint32_t tP = tmem + lane_off + (wg ? TM_P1 : TM_P0);
     const uint32_t bar_id = 1 + wg;
+    // Non-causal: turns at the exponentials, as in the bf16 forward (named
+    // barriers 3 and 4, 256 threads, tile 1 first at every key step; every warp
+    // takes one turn per key step of every item, with no work where it has
+    // none). Causal items of 2-8 steps lost 2 us with them at the GPT-2 shape.
+    constexpr bool TURNS = !CAUSAL;
+    const uint32_t my_turn = 3 + wg, next_turn = 4 - wg;
+    auto idle_turns = [&](int k) {
+      if constexpr (TURNS) {
+        for (; k > 0; --k) {
+          named_bar_sync(my_turn, 256);
+          named_bar_arrive(next_turn, 256);
+        }
+      }
+    };
     const bool leader = (warp & 3) == 0 && lane == 0;
     uint8_t* stage = smem + L::OUT_OFF + wg * L::OUT_TILE;
     const size_t dstride = (size_t)p.BH * p.nT;  // between the q, k and v descale planes
     bool ok = true;
     int gs = 0;
-    for (int ic = 0; ok && ic < n_items_cta; ++ic) {
+    if (TURNS && wg == 0) named_bar_arrive(4, 256);   // tile 1 takes the first turn
+    int ic = 0;
+    for (; ok && ic < n_items_cta; ++ic) {
       const Item w = decode<CAUSAL>(deal_item(deal, ic), p);
       const int qb = ic & 1;
       const int n = w.n_tile[wg];
@@ -300,6 +317,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
       for (int kt = 0; kt < n && dsc_in; ++kt) dv_ref = fmaxf(dv_ref, __ldg(dsc + 2 * dstride + kt));
       const float lg_dv_ref = __log2f(dv_ref);
       float m_run = -INFINITY, l_run = 0.f;
+      int turns = 0;                             // turns taken in this item
       for (int j = 0; j < n; ++j) {
         const int gj = gs + j;
         // this key tile: exponent scale of the raw e4m3 products, and
@@ -350,6 +368,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
         const float alpha = ex2_approx(m_run - m_new);
         const float2 c2 = make_float2(c, c), nmc = make_float2(a_j - m_new, a_j - m_new);
         float2 ls[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+        if (TURNS) named_bar_sync(my_turn, 256);         // this warpgroup's turn
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t pk[16];
@@ -385,6 +404,8 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
           }
           tmem_st16(tP + hf * 16, pk);
         }
+        if (TURNS) named_bar_arrive(next_turn, 256);     // the other warpgroup's turn
+        ++turns;
         if (!ok) break;
         const float lsum = ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
         l_run = l_run * alpha + lsum * ex2_approx(-a_j);   // the sum of p = p' / r_j
@@ -394,6 +415,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_p[wg]);
       }
+      idle_turns(w.n_max - turns);
       // ---------------------------------------------------------- epilogue of this item
       // A warp whose wait gave up left the key loop early, but it still comes
       // here: failures are combined over the warpgroup at the barrier below, so
@@ -433,6 +455,11 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_co
       if (leader && ic + 2 < n_items_cta) mbar_arrive(&bar_q_empty[qb]);
       gs += n;
     }
+    // after a failure: the turns of the items not walked (the failed item's
+    // were all taken before its epilogue)
+    if (TURNS)
+      for (++ic; ic < n_items_cta; ++ic) idle_turns(decode<CAUSAL>(deal_item(deal, ic), p).n_max);
+    if (TURNS && wg == 1) named_bar_sync(4, 256);   // the other warpgroup's last hand-over
     if (leader) bulk_wait_group0();
   }
 
