@@ -162,9 +162,10 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
   E* sK = reinterpret_cast<E*>(sbase + (MMA ? P_TILE_BYTES : 0));
   E* sV = sK + CH * HS;
   E* sQ = sV + CH * HS;                         // MMA path: 16 query rows
-  __shared__ float sp[TQ][CH];
+  __shared__ float sp[MMA ? 1 : TQ][MMA ? 1 : CH];   // CUDA-core path: scores, then p
   __shared__ float red[TQ][THREADS / 32];
   __shared__ float row_m[TQ];
+  __shared__ float red_l[MMA ? TQ : 1][THREADS / 32];   // tensor-core path: row sums per warp
   __shared__ float sacc[MMA ? 1 : THREADS / 32][MMA ? 1 : TQ][MMA ? 1 : HS];
   __shared__ uint64_t bar_k, bar_v, bar_s, bar_o;
   __shared__ uint32_t tmem_sh;
@@ -238,17 +239,100 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
       mma_commit(&bar_s);
     }
     ok = mbar_wait(&bar_s, 0, &abort_sh, p.err) && ok;
+    // this thread's key j: its scaled scores for the Tq queries (log2 units)
+    const int j = tid;                                // key of this thread = TMEM lane
+    float xs[TQ];
+#pragma unroll
+    for (int i = 0; i < TQ; ++i) xs[i] = -INFINITY;
     if (ok) {
       tc_fence_after();
       uint32_t sc[16];
       tmem_ld16_wait(tmem + ((uint32_t)(warp * 32) << 16), sc);
-      const int j = tid;                              // key of this thread = TMEM lane
 #pragma unroll
       for (int i = 0; i < TQ; ++i)
-        if (i < Tq)
-          sp[i][j] = (j < nk && j0 + j <= L - Tq + i) ? __uint_as_float(sc[i]) * p.scale_log2 : -INFINITY;
+        if (i < Tq && j < nk && j0 + j <= L - Tq + i) xs[i] = __uint_as_float(sc[i]) * p.scale_log2;
     }
     tc_fence_before();                              // S^T read: O may overwrite its columns
+    // chunk-local softmax per query from registers: warp maxima, then the
+    // four warps' through red; exponentials as bf16 P; warp sums into red_l
+#pragma unroll
+    for (int i = 0; i < TQ; ++i) {
+      if (i < Tq) {
+        float m = xs[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) red[i][warp] = m;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < TQ; ++i) {
+      if (i < Tq) {
+        float m = red[i][0];
+#pragma unroll
+        for (int w = 1; w < THREADS / 32; ++w) m = fmaxf(m, red[i][w]);
+        const float e = m == -INFINITY ? 0.f : ex2_approx(xs[i] - m);
+        // P[i][j] (bf16) at row i of key half j/64, chunk (j%64)/8 swizzled by row
+        const int kk = j & 63;
+        *reinterpret_cast<uint16_t*>(sP + (j >> 6) * (16 * 128) + i * 128 + ((((kk >> 3) ^ (i & 7)) << 4)) +
+                                     (kk & 7) * 2) = (uint16_t)(pack_bf16x2(e, 0.f) & 0xFFFFu);
+        float l = e;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) red_l[i][warp] = l;
+        if (tid == i) row_m[i] = m;
+      }
+    }
+    fence_proxy_async_smem();                         // P is read by the tensor core
+    __syncthreads();
+    ok = mbar_wait(&bar_v, 0, &abort_sh, p.err) && ok;
+    // O = P V: A = P (K-major, the second key half 2 KB on), B = V (MN-major)
+    if (tid == 0 && ok) {
+      tc_fence_after();
+      const uint64_t dp = make_sdesc(smem_u32(sP), 16, 1024, SWZ_128B);
+      const uint64_t dv = make_sdesc(smem_u32(sV), 16, G::ATOM_BYTES, G::SWZ);
+      constexpr uint32_t idesc = make_idesc_bf16(CH, HS, false, true);
+#pragma unroll
+      for (int k = 0; k < CH / 16; ++k)
+        mma_ss(tmem, desc_add(dp, (k >> 2) * (16 * 128) + (k & 3) * 32),
+               desc_add(dv, k * 16 * G::ROW_BYTES), idesc, k > 0);
+      mma_commit(&bar_o);
+    }
+    ok = mbar_wait(&bar_o, 0, &abort_sh, p.err) && ok;
+    if (warp == 0 && ok) {
+      // query rows = TMEM lanes 0..Tq-1: m (log2 units), l, o[HS]
+      tc_fence_after();
+      uint32_t o[HS];
+#pragma unroll
+      for (int c0 = 0; c0 < HS; c0 += 16) {
+        uint32_t t16[16];
+        tmem_ld16_wait(tmem + c0, t16);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) o[c0 + k] = t16[k];
+      }
+      if (lane < Tq) {
+        float* rec = p.part + (((size_t)bh * p.n_split + split) * Tq + lane) * (HS + 2);
+        float l = 0.f;
+#pragma unroll
+        for (int w = 0; w < THREADS / 32; ++w) l += red_l[lane][w];
+        rec[0] = row_m[lane];
+        rec[1] = l;
+        // records are HS + 2 floats long: 8-byte aligned, so pairs
+#pragma unroll
+        for (int d = 0; d < HS; d += 2)
+          *reinterpret_cast<float2*>(rec + 2 + d) = make_float2(__uint_as_float(o[d]), __uint_as_float(o[d + 1]));
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      // a wait that gave up may leave a group in flight: let it land first
+      if (abort_sh)
+        for (int k = 0; k < 1000; ++k) __nanosleep(1000);
+      __syncwarp();
+      tmem_dealloc(tmem, TMEM_COLS);
+    }
+    return;
   } else
   // scores: packed partial dot products over the lane's 8 columns, then the
   // transposing butterfly over the row's lanes
@@ -297,72 +381,15 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
     float l = 0.f;
     for (int j = tid; j < CH; j += THREADS) {
       const float e = m == -INFINITY ? 0.f : ex2_approx(sp[i][j] - m);
-      if constexpr (MMA) {
-        // P[i][j] (bf16) at row i of key half j/64, chunk (j%64)/8 swizzled by row
-        const int kk = j & 63;
-        *reinterpret_cast<uint16_t*>(sP + (j >> 6) * (16 * 128) + i * 128 + ((((kk >> 3) ^ (i & 7)) << 4)) +
-                                     (kk & 7) * 2) = (uint16_t)(pack_bf16x2(e, 0.f) & 0xFFFFu);
-      } else {
-        sp[i][j] = e;
-      }
+      sp[i][j] = e;
       l += e;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     if (lane == 0) red[i][warp] = l;
   }
-  if constexpr (MMA) fence_proxy_async_smem();     // P is read by the tensor core
   __syncthreads();
   ok = mbar_wait(&bar_v, 0, &abort_sh, p.err) && ok;
-  if constexpr (MMA) {
-    // O = P V: A = P (K-major, the second key half 2 KB on), B = V (MN-major)
-    if (tid == 0 && ok) {
-      tc_fence_after();
-      const uint64_t dp = make_sdesc(smem_u32(sP), 16, 1024, SWZ_128B);
-      const uint64_t dv = make_sdesc(smem_u32(sV), 16, G::ATOM_BYTES, G::SWZ);
-      constexpr uint32_t idesc = make_idesc_bf16(CH, HS, false, true);
-#pragma unroll
-      for (int k = 0; k < CH / 16; ++k)
-        mma_ss(tmem, desc_add(dp, (k >> 2) * (16 * 128) + (k & 3) * 32),
-               desc_add(dv, k * 16 * G::ROW_BYTES), idesc, k > 0);
-      mma_commit(&bar_o);
-    }
-    ok = mbar_wait(&bar_o, 0, &abort_sh, p.err) && ok;
-    if (warp == 0 && ok) {
-      // query rows = TMEM lanes 0..Tq-1: m (log2 units), l, o[HS]
-      tc_fence_after();
-      uint32_t o[HS];
-#pragma unroll
-      for (int c0 = 0; c0 < HS; c0 += 16) {
-        uint32_t t16[16];
-        tmem_ld16_wait(tmem + c0, t16);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) o[c0 + k] = t16[k];
-      }
-      if (lane < Tq) {
-        float* rec = p.part + (((size_t)bh * p.n_split + split) * Tq + lane) * (HS + 2);
-        float l = 0.f;
-#pragma unroll
-        for (int w = 0; w < THREADS / 32; ++w) l += red[lane][w];
-        rec[0] = row_m[lane];
-        rec[1] = l;
-        // records are HS + 2 floats long: 8-byte aligned, so pairs
-#pragma unroll
-        for (int d = 0; d < HS; d += 2)
-          *reinterpret_cast<float2*>(rec + 2 + d) = make_float2(__uint_as_float(o[d]), __uint_as_float(o[d + 1]));
-      }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-      // a wait that gave up may leave a group in flight: let it land first
-      if (abort_sh)
-        for (int k = 0; k < 1000; ++k) __nanosleep(1000);
-      __syncwarp();
-      tmem_dealloc(tmem, TMEM_COLS);
-    }
-    return;
-  }
   // partial outputs: each lane accumulates its 8 columns over its rows of the
   // chunk for every query (packed pairs), then the transposing butterfly sums
   // the rows of the warp and the warps are summed through shared memory
