@@ -13,8 +13,9 @@ every poll and non-blocking polls (mbarrier.test_wait; the product build's
 try_wait may suspend until the phase completes), so their first wait that is
 not over within about a microsecond runs out, in whichever role it happens.
 In a child process that copy runs a forward and a backward with several work
-items per CTA; each must return, the host must read ATTN_ERR_TIMEOUT once per
-call, and no CUDA error may follow. The parent then runs the normal library
+items per CTA, an fp32-input forward and a non-causal FP8 forward; each must
+return, the host must read ATTN_ERR_TIMEOUT once per call, and no CUDA error
+may follow. The parent then runs the normal library
 on the same GPU and checks its results against the oracle.
 """
 import json
@@ -102,6 +103,22 @@ r["bwd_status"] = lib.attn_bwd(dout.data_ptr(), qkv.data_ptr(), out.data_ptr(), 
 torch.cuda.synchronize()
 r["bwd_error"] = lib.attn_last_device_error(s)
 r["after"] = lib.attn_last_device_error(s)
+# the fp32-input forward and the non-causal FP8 forward (their softmax
+# warpgroups take turns through named barriers, which must pair up however
+# the waits give up)
+q32 = torch.randn(B, T, 3 * C, device="cuda", generator=g) * 0.5
+o32 = torch.empty(B, T, C, device="cuda")
+r["f32_status"] = lib.attn_fwd(q32.data_ptr(), o32.data_ptr(), lse.data_ptr(), B, T, C, NH, 1, 0, s)
+torch.cuda.synchronize()
+r["f32_error"] = lib.attn_last_device_error(s)
+lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
+lib.attn_fwd_fp8.restype = i
+nT = (T + 127) // 128
+codes = torch.randn(B, T, 3 * C, device="cuda", generator=g).to(torch.float8_e4m3fn).view(torch.uint8)
+desc = (torch.rand(3, B, NH, nT, device="cuda", generator=g) + 0.5) * 0.25
+r["fp8_status"] = lib.attn_fwd_fp8(codes.data_ptr(), desc.data_ptr(), out.data_ptr(), lse.data_ptr(), B, T, C, NH, 0, s)
+torch.cuda.synchronize()
+r["fp8_error"] = lib.attn_last_device_error(s)
 print(json.dumps(r))
 """
 
@@ -123,6 +140,8 @@ def test_real_kernels_wind_down_when_their_waits_run_out(env):
     assert res["fwd_error"] == api.ATTN_ERR_TIMEOUT                                  # gave up, reported
     assert res["bwd_error"] == api.ATTN_ERR_TIMEOUT
     assert res["after"] == api.ATTN_OK                                               # the read cleared it
+    assert res["f32_status"] == api.ATTN_OK and res["f32_error"] == api.ATTN_ERR_TIMEOUT
+    assert res["fp8_status"] == api.ATTN_OK and res["fp8_error"] == api.ATTN_ERR_TIMEOUT
     # the GPU still runs the normal library's kernels correctly
     assert api.attn_last_device_error() == api.ATTN_OK
     B, T, C, NH = 2, 300, 128, 2
