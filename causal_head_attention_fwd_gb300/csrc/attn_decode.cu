@@ -451,10 +451,15 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
 }
 
 // One warp per (b, h, query), four per block: merge the chunks' partials.
-// The chunk maxima and row sums are read one chunk per lane; the outputs,
-// HS/32 columns per lane, with four chunks' loads in flight at a time.
+// PER_LANE (one query token): each lane takes every 32nd chunk record (all of
+// a record's loads are independent, so the set is fetched in about one round
+// trip), sums its records' outputs weighted by 2^(m_s - M), and a transposing
+// butterfly over the lanes leaves columns 2*lane, 2*lane+1 (hs 64) or lane
+// (hs 32) in each lane. Otherwise (several queries, 8x the warps) the warp
+// walks the records in order, hs/32 columns per lane and four records' loads
+// in flight, so every load is a whole record row.
 constexpr int COMBINE_WARPS = 4;
-template <typename E, int HS>
+template <typename E, int HS, bool PER_LANE>
 __global__ void __launch_bounds__(32 * COMBINE_WARPS) attn_decode_combine(const Params p) {
   constexpr int DPL = HS / 32;                       // output columns per lane
   const int lane = threadIdx.x & 31;
@@ -472,45 +477,82 @@ __global__ void __launch_bounds__(32 * COMBINE_WARPS) attn_decode_combine(const 
   for (int s = lane; s < n; s += 32) M = fmaxf(M, rec[s * stride]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float l = 0.f;
-  for (int s = lane; s < n; s += 32) l = fmaf(rec[s * stride + 1], ex2_approx(rec[s * stride] - M), l);
+  if constexpr (!PER_LANE) {
+    float l = 0.f;
+    for (int s = lane; s < n; s += 32) l = fmaf(rec[s * stride + 1], ex2_approx(rec[s * stride] - M), l);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-  float acc[DPL];
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    float acc[DPL];
 #pragma unroll
-  for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
-  int s = 0;
-  for (; s + 4 <= n; s += 4) {
-    float w[4], v[4][DPL];
+    for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
+    int s = 0;
+    for (; s + 4 <= n; s += 4) {
+      float w[4], v[4][DPL];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float* r = rec + (s + u) * stride;
-      w[u] = r[0];
+      for (int u = 0; u < 4; ++u) {
+        const float* r = rec + (s + u) * stride;
+        w[u] = r[0];
 #pragma unroll
-      for (int k = 0; k < DPL; ++k) v[u][k] = r[2 + k * 32 + lane];
+        for (int k = 0; k < DPL; ++k) v[u][k] = r[2 + k * 32 + lane];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float wu = ex2_approx(w[u] - M);
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) acc[k] = fmaf(v[u][k], wu, acc[k]);
+      }
+    }
+    for (; s < n; ++s) {
+      const float* r = rec + s * stride;
+      const float wu = ex2_approx(r[0] - M);
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) acc[k] = fmaf(r[2 + k * 32 + lane], wu, acc[k]);
+    }
+    const float inv_l = 1.f / l;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) {
+      const float val = acc[k] * inv_l;
+      const size_t oi = ((size_t)b * Tq + i) * p.C + h * HS + k * 32 + lane;
+      if constexpr (sizeof(E) == 4) static_cast<float*>(p.out)[oi] = val;
+      else static_cast<uint16_t*>(p.out)[oi] = (uint16_t)(pack_bf16x2(val, 0.f) & 0xFFFFu);
+    }
+    if (lane == 0) p.lse[(size_t)bh * Tq + i] = (M + __log2f(l)) * 0.69314718055994531f;
+  } else {
+    float acc[HS];
+#pragma unroll
+    for (int d = 0; d < HS; ++d) acc[d] = 0.f;
+    float l = 0.f;
+    for (int s = lane; s < n; s += 32) {
+      const float* r = rec + s * stride;
+      float v[HS];
+#pragma unroll
+      for (int d = 0; d < HS; d += 2) {                // records are 8-byte aligned
+        const float2 x = *reinterpret_cast<const float2*>(r + 2 + d);
+        v[d] = x.x;
+        v[d + 1] = x.y;
+      }
+      const float w = ex2_approx(r[0] - M);
+      l = fmaf(r[1], w, l);
+#pragma unroll
+      for (int d = 0; d < HS; ++d) acc[d] = fmaf(v[d], w, acc[d]);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float wu = ex2_approx(w[u] - M);
-#pragma unroll
-      for (int k = 0; k < DPL; ++k) acc[k] = fmaf(v[u][k], wu, acc[k]);
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    int first = 0;
+    TRed<HS, HS, 16, 1>::run(acc, lane, first);        // acc[0..DPL): columns first, first+1, ...
+    const float inv_l = 1.f / l;
+    const size_t oi = ((size_t)b * Tq + i) * p.C + h * HS + first;
+    if constexpr (DPL == 2) {
+      if constexpr (sizeof(E) == 4)
+        *reinterpret_cast<float2*>(static_cast<float*>(p.out) + oi) = make_float2(acc[0] * inv_l, acc[1] * inv_l);
+      else
+        *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + oi) = pack_bf16x2(acc[0] * inv_l, acc[1] * inv_l);
+    } else {
+      if constexpr (sizeof(E) == 4) static_cast<float*>(p.out)[oi] = acc[0] * inv_l;
+      else static_cast<uint16_t*>(p.out)[oi] = (uint16_t)(pack_bf16x2(acc[0] * inv_l, 0.f) & 0xFFFFu);
     }
+    if (lane == 0) p.lse[(size_t)bh * Tq + i] = (M + __log2f(l)) * 0.69314718055994531f;
   }
-  for (; s < n; ++s) {
-    const float* r = rec + s * stride;
-    const float wu = ex2_approx(r[0] - M);
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) acc[k] = fmaf(r[2 + k * 32 + lane], wu, acc[k]);
-  }
-  const float inv_l = 1.f / l;
-#pragma unroll
-  for (int k = 0; k < DPL; ++k) {
-    const float val = acc[k] * inv_l;
-    const size_t oi = ((size_t)b * Tq + i) * p.C + h * HS + k * 32 + lane;
-    if constexpr (sizeof(E) == 4) static_cast<float*>(p.out)[oi] = val;
-    else static_cast<uint16_t*>(p.out)[oi] = (uint16_t)(pack_bf16x2(val, 0.f) & 0xFFFFu);
-  }
-  if (lane == 0) p.lse[(size_t)bh * Tq + i] = (M + __log2f(l)) * 0.69314718055994531f;
 }
 
 template <typename E, int HS>
@@ -525,8 +567,8 @@ static cudaError_t launch_t(const CUtensorMap& m, const CUtensorMap& mkq, const 
   k<<<(unsigned)(BH * p.n_split), THREADS, smem, s>>>(m, mkq, mq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_decode_combine<E, HS><<<(unsigned)((BH * p.Tq + COMBINE_WARPS - 1) / COMBINE_WARPS), 32 * COMBINE_WARPS, 0,
-                                 s>>>(p);
+  auto c = p.Tq == 1 ? attn_decode_combine<E, HS, true> : attn_decode_combine<E, HS, false>;
+  c<<<(unsigned)((BH * p.Tq + COMBINE_WARPS - 1) / COMBINE_WARPS), 32 * COMBINE_WARPS, 0, s>>>(p);
   return cudaGetLastError();
 }
 
