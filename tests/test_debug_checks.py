@@ -99,6 +99,8 @@ def dec(lib):
                                          ws.data_ptr(), n, s))
     return out, lse
 both("decode", dec)
+Tq = 1
+both("decode one token", dec)
 
 # FP8 forward and backward
 B, T, C, NH = 2, 300, 128, 2
@@ -110,12 +112,15 @@ def fp8(lib):
     out = torch.empty(B, T, C, dtype=torch.bfloat16, device=dev); lse = torch.empty(B, NH, T, device=dev)
     res["status"].append(lib.attn_fwd_fp8(codes.data_ptr(), desc.data_ptr(), out.data_ptr(), lse.data_ptr(),
                                           B, T, C, NH, 1, s))
+    out_nc = torch.empty_like(out); lse_nc = torch.empty_like(lse)          # no mask: turns at the exponentials
+    res["status"].append(lib.attn_fwd_fp8(codes.data_ptr(), desc.data_ptr(), out_nc.data_ptr(), lse_nc.data_ptr(),
+                                          B, T, C, NH, 0, s))
     dqkv = torch.empty(B, T, 3 * C, dtype=torch.bfloat16, device=dev)
     n = lib.attn_bwd_fp8_workspace_size(B, T, C, NH, 1)
     ws = torch.empty(n, dtype=torch.uint8, device=dev)
     res["status"].append(lib.attn_bwd_fp8(dout.data_ptr(), codes.data_ptr(), desc.data_ptr(), out.data_ptr(),
                                           lse.data_ptr(), dqkv.data_ptr(), B, T, C, NH, 1, ws.data_ptr(), n, s))
-    return out, lse, dqkv
+    return out, lse, dqkv, out_nc, lse_nc
 both("fp8", fp8)
 
 # linear
