@@ -55,6 +55,8 @@ def test_decode_rejects_bad_arguments(env):
     (1, 512, 128, 2, 5), (3, 1000, 128, 2, 2), (1, 256, 128, 2, 1),
     # caches shorter than the 16 query rows the tensor-core form loads
     (1, 5, 128, 2, 4), (2, 3, 128, 4, 3),
+    # hs 32, one query token: the combine's one-record-per-lane form, one column per lane
+    (2, 300, 128, 4, 1), (1, 4100, 64, 2, 1),
 ])
 def test_decode_matches_last_rows_of_the_full_forward(env, dtype, B, L, C, NH, Tq):
     torch, api, ops = env
