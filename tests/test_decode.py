@@ -57,6 +57,8 @@ def test_decode_rejects_bad_arguments(env):
     (1, 5, 128, 2, 4), (2, 3, 128, 4, 3),
     # hs 32, one query token: the combine's one-record-per-lane form, one column per lane
     (2, 300, 128, 4, 1), (1, 4100, 64, 2, 1),
+    # hs 32 with more than four query tokens (the 8-query instantiation)
+    (1, 700, 128, 4, 7),
 ])
 def test_decode_matches_last_rows_of_the_full_forward(env, dtype, B, L, C, NH, Tq):
     torch, api, ops = env
