@@ -491,7 +491,8 @@ def run_decode(args):
                        "l2": "flushed between timed steps (512 MiB write)"},
             "roofline": {"kernel": "attn_decode_split", "bound": "hbm", "achieved": gbs,
                          "peak": float(peaks["hbm_gbs"]), "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]),
-                         "traffic": None, "peak_source": f"{src} HBM copy (MEASURED_PEAKS.json hbm_gbs)"},
+                         "traffic": stored_traffic("attn_decode_split", w.name),
+                         "peak_source": f"{src} HBM copy (MEASURED_PEAKS.json hbm_gbs)"},
             "bytes_per_step": nbytes, "cache_bytes": cache, "tokens_per_s": B * Tq / (t_ms * 1e-3),
             "gpu_launches": 2 * args.steps, "clocks": cs.summary()}
     print(json.dumps(line), flush=True)
@@ -636,11 +637,7 @@ def main(argv=None):
     else:
         roofline = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": float(peaks["hbm_gbs"]),
                     "unit": "GB/s", "frac": None, "traffic": None}
-    traffic_file = ROOT / "profiles" / "traffic.json"
-    if traffic_file.exists():
-        tr = json.loads(traffic_file.read_text()).get(dom)
-        if tr and tr.get("source_hash") == kernel_source_hash(dom):
-            roofline["traffic"] = tr["bytes_per_launch"]
+    roofline["traffic"] = stored_traffic(dom, w.name)
     names = list(kern)
     fwd_ms = kern[names[0]]["avg_ms"]
     bwd_ms = sum(kern[k]["avg_ms"] for k in names[1:])
@@ -733,8 +730,22 @@ def main(argv=None):
 _KERNEL_SOURCES = {
     "attn_fwd_kernel": ["attn_fwd.cu", "fwd_deal.cuh", "common.cuh", "ptx.cuh"],
     "attn_bwd_kernel": ["attn_bwd.cu", "fwd_deal.cuh", "common.cuh", "ptx.cuh"],
+    "attn_decode_split": ["attn_decode.cu", "common.cuh", "ptx.cuh"],
     "f32": ["attn_f32.cu", "tf32.cuh", "common.cuh", "ptx.cuh"],
 }
+
+
+def stored_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from one ncu capture
+    (profiles/traffic.json, key "<kernel>@<workload>"), or None when there is
+    no capture of this workload or the kernel's code has changed since."""
+    f = ROOT / "profiles" / "traffic.json"
+    if not f.exists():
+        return None
+    tr = json.loads(f.read_text()).get(f"{kernel}@{workload}")
+    if tr and tr.get("source_hash") == kernel_source_hash(kernel):
+        return tr["bytes_per_launch"]
+    return None
 
 
 def _code_only(text: str) -> str:
