@@ -111,6 +111,7 @@ MULTI_ITEM = [
     (16, 512, 256, 8, 1),       # hs 32, causal: 256 / 512
     (8, 600, 256, 8, 0),        # hs 32, no mask: 192 / 320 (snake order)
     (6, 1000, 768, 12, 0),      # hs 64, no mask, ragged tail: 288 / 576
+    (6, 1100, 768, 12, 1),      # hs 64, causal, the last pair's second tile past T: 360 / 648
 ]
 
 
