@@ -151,6 +151,22 @@ def test_fp8_forward_matches_oracle(env, B, T, C, NH, causal, gain):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("B,T,C,NH", [
+    (8, 600, 768, 12),        # hs 64: 288 items for 152 CTAs, the last pair's second tile past T
+    (16, 300, 256, 8),        # hs 32: 256 items
+])
+def test_fp8_noncausal_several_items_per_cta_all_heads(env, B, T, C, NH):
+    """Without the mask the two softmax warpgroups take turns at the
+    exponentials; every head against the oracle where each persistent CTA walks
+    several items, some with one tile past T (that warpgroup's turns idle)."""
+    f = inputs.make_fp8_inputs(B, T, C, sigma=0.5, seed=91 + T, NH=NH)
+    g_out, g_lse = _run(env, f, B, T, C, NH, 0)
+    for b in range(B):
+        for h in range(NH):
+            _check_head(g_out, g_lse, f.qkv, b, h, T, C, NH, False)
+
+
+@pytest.mark.gpu
 def test_fp8_gpt2s_workload_all_heads(env):
     """The FP8 benchmark's shape (B=16, T=1024, C=768, NH=12): every head against
     the oracle on the dequantised inputs, and the whole output written."""
