@@ -451,13 +451,14 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
 }
 
 // One warp per (b, h, query), four per block: merge the chunks' partials.
-// PER_LANE (one query token): each lane takes every 32nd chunk record (all of
-// a record's loads are independent, so the set is fetched in about one round
-// trip), sums its records' outputs weighted by 2^(m_s - M), and a transposing
-// butterfly over the lanes leaves columns 2*lane, 2*lane+1 (hs 64) or lane
-// (hs 32) in each lane. Otherwise (several queries, 8x the warps) the warp
-// walks the records in order, hs/32 columns per lane and four records' loads
-// in flight, so every load is a whole record row.
+// PER_LANE (up to four query tokens): each lane takes every 32nd chunk record
+// (all of a record's loads are independent, so the set is fetched in about one
+// round trip), sums its records' outputs weighted by 2^(m_s - M), and a
+// transposing butterfly over the lanes leaves columns 2*lane, 2*lane+1 (hs 64)
+// or lane (hs 32) in each lane. Otherwise (five to eight queries, more warps
+// than the GPU holds at once) the warp walks the records in order, hs/32
+// columns per lane and four records' loads in flight, so every load is a whole
+// record row.
 constexpr int COMBINE_WARPS = 4;
 template <typename E, int HS, bool PER_LANE>
 __global__ void __launch_bounds__(32 * COMBINE_WARPS) attn_decode_combine(const Params p) {
@@ -567,7 +568,7 @@ static cudaError_t launch_t(const CUtensorMap& m, const CUtensorMap& mkq, const 
   k<<<(unsigned)(BH * p.n_split), THREADS, smem, s>>>(m, mkq, mq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto c = p.Tq == 1 ? attn_decode_combine<E, HS, true> : attn_decode_combine<E, HS, false>;
+  auto c = p.Tq <= 4 ? attn_decode_combine<E, HS, true> : attn_decode_combine<E, HS, false>;
   c<<<(unsigned)((BH * p.Tq + COMBINE_WARPS - 1) / COMBINE_WARPS), 32 * COMBINE_WARPS, 0, s>>>(p);
   return cudaGetLastError();
 }

@@ -55,8 +55,8 @@ def test_decode_rejects_bad_arguments(env):
     (1, 512, 128, 2, 5), (3, 1000, 128, 2, 2), (1, 256, 128, 2, 1),
     # caches shorter than the 16 query rows the tensor-core form loads
     (1, 5, 128, 2, 4), (2, 3, 128, 4, 3),
-    # hs 32, one query token: the combine's one-record-per-lane form, one column per lane
-    (2, 300, 128, 4, 1), (1, 4100, 64, 2, 1),
+    # hs 32, one to four query tokens: the combine's one-record-per-lane form, one column per lane
+    (2, 300, 128, 4, 1), (1, 4100, 64, 2, 1), (1, 2100, 64, 2, 4),
     # hs 32 with more than four query tokens (the 8-query instantiation)
     (1, 700, 128, 4, 7),
 ])
