@@ -28,7 +28,8 @@ Coverage: every head of small shapes (one tile, several tiles, ragged tails,
 hs 32 and 64, causal and not); every head of shapes whose persistent kernels
 give each CTA several work items (the forward's causal deal table, its snake
 order without the mask, the backward's snake order, the Q double buffer and the
-K/V rings running on across items); and every head of the full GPT-2 small
+K/V rings running on across items), also with more causal items than the deal
+table holds (both kernels in the snake order); and every head of the full GPT-2 small
 (fp32 and bf16), GPT-2 XL-width and ViT-B/16 workloads, with four heads over
 both sequences of the long-context one, in the benchmark's launch configuration.
 """
@@ -147,6 +148,17 @@ def test_parity_all_heads_several_items_per_cta(env, B, T, C, NH, causal, dtype)
     assert B * NH * ((T + 255) // 256) > n_sm
     host, out, lse, dqkv = _run(env, B, T, C, NH, causal, dtype=dtype, seed=3 * T + NH)
     _check(host, out, lse, dqkv, B, T, C, NH, causal, dtype)
+
+
+def test_parity_causal_beyond_the_deal_table(env):
+    """Causal items of unequal length, more than the 2048 the host's deal
+    table holds: both persistent kernels fall back to the snake order
+    (hs 32: 2080 forward items of 1 and 2 key steps per query tile, 4160
+    backward items of 1 to 4 steps). Every head against the oracle."""
+    B, T, C, NH = 260, 512, 128, 4
+    assert B * NH * ((T + 255) // 256) > 2048 and B * NH * ((T + 127) // 128) > 2048
+    host, out, lse, dqkv = _run(env, B, T, C, NH, 1, seed=5 * B + T)
+    _check(host, out, lse, dqkv, B, T, C, NH, 1, "bf16")
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
