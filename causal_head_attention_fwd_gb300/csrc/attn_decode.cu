@@ -113,23 +113,28 @@ __host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x
 // core. S^T = K Q^T for the chunk's 128 keys (TMEM lanes) and the queries
 // padded to 16 (columns), one tcgen05 group of hs/16 instructions, read back
 // one key row per thread. The exponentials go to shared memory as bf16 P,
-// rows = queries, K-major in the 128-byte swizzle (16 rows of each 64-key
-// half are written; the rows past them that the M = 128 product reads are
-// other data, and only output rows below Tq are used), and O = P V is a
-// second group (N = hs, 8 instructions, over the columns S^T held) whose
-// rows warp 0 reads from TMEM. 64 TMEM columns per CTA.
+// rows = queries, K-major in the 128-byte swizzle (one 8-row atom per 64-key
+// half, the rows below Tq written; the rows past them that the M = 128
+// product reads are other data, and only output rows below Tq are used), and
+// O = P V is a second group (N = hs, 8 instructions, over the columns S^T
+// held) whose rows warp 0 reads from TMEM. 64 TMEM columns per CTA.
 // K, V and the queries arrive by swizzled tensor copies (map_kq: box
-// {hs, 128 rows}, map_q: box {hs, 16 rows}). One query token, or fp32 inputs,
-// keep both products on the FMA pipe (exact fp32 products).
+// {hs, 128 rows}, map_q: box {hs, 16 rows}). The 16 query rows sit where P
+// is written later (S^T has been computed from them by then), so a CTA holds
+// 2 KB + its 32 KB chunk and six CTAs fit an SM. One query token, or fp32
+// inputs, keep both products on the FMA pipe (exact fp32 products).
 template <typename E, int HS, int TQ>
 struct DecodeMma {
   static constexpr bool on = sizeof(E) == 2 && TQ > 1;
 };
-constexpr int P_TILE_BYTES = 2 * 16 * 128;      // P: 2 key halves x 16 query rows x 128 bytes
+constexpr int P_ROWS = 8;                       // query rows of P per key half: one swizzle atom
+constexpr int P_TILE_BYTES = 2 * P_ROWS * 128;  // P: 2 key halves x 8 query rows x 128 bytes
 constexpr int TMEM_COLS = 64;                   // S^T (16 columns), then O over them (hs columns)
 template <typename E, int HS, int TQ>
 __host__ __device__ constexpr int split_smem_bytes() {
-  return DecodeMma<E, HS, TQ>::on ? P_TILE_BYTES + 2 * Chunk<E>::N * HS * (int)sizeof(E) + 16 * HS * 2 + 1024
+  static_assert(!DecodeMma<E, HS, TQ>::on || (TQ <= P_ROWS && 16 * HS * 2 <= P_TILE_BYTES),
+                "P rows hold every query; the 16 query rows fit where P goes");
+  return DecodeMma<E, HS, TQ>::on ? P_TILE_BYTES + 2 * Chunk<E>::N * HS * (int)sizeof(E) + 1024
                                   : 2 * Chunk<E>::N * HS * (int)sizeof(E) + 128;
 }
 
@@ -161,7 +166,7 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
   uint8_t* sP = sbase;                          // MMA path only
   E* sK = reinterpret_cast<E*>(sbase + (MMA ? P_TILE_BYTES : 0));
   E* sV = sK + CH * HS;
-  E* sQ = sV + CH * HS;                         // MMA path: 16 query rows
+  E* sQ = reinterpret_cast<E*>(sP);             // MMA path: 16 query rows, overwritten by P once S^T is done
   __shared__ float sp[MMA ? 1 : TQ][MMA ? 1 : CH];   // CUDA-core path: scores, then p
   __shared__ float red[TQ][THREADS / 32];
   __shared__ float row_m[TQ];
@@ -274,7 +279,7 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
         const float e = m == -INFINITY ? 0.f : ex2_approx(xs[i] - m);
         // P[i][j] (bf16) at row i of key half j/64, chunk (j%64)/8 swizzled by row
         const int kk = j & 63;
-        *reinterpret_cast<uint16_t*>(sP + (j >> 6) * (16 * 128) + i * 128 + ((((kk >> 3) ^ (i & 7)) << 4)) +
+        *reinterpret_cast<uint16_t*>(sP + (j >> 6) * (P_ROWS * 128) + i * 128 + ((((kk >> 3) ^ (i & 7)) << 4)) +
                                      (kk & 7) * 2) = (uint16_t)(pack_bf16x2(e, 0.f) & 0xFFFFu);
         float l = e;
 #pragma unroll
@@ -286,7 +291,7 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
     fence_proxy_async_smem();                         // P is read by the tensor core
     __syncthreads();
     ok = mbar_wait(&bar_v, 0, &abort_sh, p.err) && ok;
-    // O = P V: A = P (K-major, the second key half 2 KB on), B = V (MN-major)
+    // O = P V: A = P (K-major, the second key half one atom on), B = V (MN-major)
     if (tid == 0 && ok) {
       tc_fence_after();
       const uint64_t dp = make_sdesc(smem_u32(sP), 16, 1024, SWZ_128B);
@@ -294,7 +299,7 @@ attn_decode_split(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
       constexpr uint32_t idesc = make_idesc_bf16(CH, HS, false, true);
 #pragma unroll
       for (int k = 0; k < CH / 16; ++k)
-        mma_ss(tmem, desc_add(dp, (k >> 2) * (16 * 128) + (k & 3) * 32),
+        mma_ss(tmem, desc_add(dp, (k >> 2) * (P_ROWS * 128) + (k & 3) * 32),
                desc_add(dv, k * 16 * G::ROW_BYTES), idesc, k > 0);
       mma_commit(&bar_o);
     }
